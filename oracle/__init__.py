@@ -1,0 +1,299 @@
+"""CPU oracle for partition-aware ZeRO averaging + sharded AdamW -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package. It wraps ``zr_oracle.c`` (plain single-threaded C, no
+FMA contraction) with numpy marshalling, plus ``brute.py`` (pure-Python exact
+arithmetic for tiny cases). It shares no code with the CUDA library.
+
+Every function below calls straight into the C file, which cites the passage of
+the pages each step follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "zr_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libzr_oracle.so")
+_CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall"]
+
+BF16, FP32 = 0, 1
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cc = os.environ.get("CC", "gcc")
+        subprocess.run([cc, *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        _declare(_lib)
+    return _lib
+
+
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+
+
+def _declare(L):
+    L.zro_layout.restype = ctypes.c_int
+    L.zro_layout.argtypes = [_vp, _i64, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.zro_bucket_pack.restype = ctypes.c_int
+    L.zro_bucket_pack.argtypes = [_vp, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _i32, _vp]
+    L.zro_reduce_scatter_avg.restype = ctypes.c_int
+    L.zro_reduce_scatter_avg.argtypes = [_i32, _i64, _i64, _i64, _vp, _i32, _f32, _vp]
+    L.zro_allreduce_avg.restype = ctypes.c_int
+    L.zro_allreduce_avg.argtypes = [_i32, _i64, _vp, _i32, _f32, _vp]
+    L.zro_grad_accumulate.restype = ctypes.c_int
+    L.zro_grad_accumulate.argtypes = [_i64, _vp, _vp, _i32]
+    L.zro_adamw_scalars.restype = ctypes.c_int
+    L.zro_adamw_scalars.argtypes = [_f32, _f32, _f32, _f32, _f32, _i64, _vp]
+    L.zro_adamw.restype = ctypes.c_int
+    L.zro_adamw.argtypes = [_i64, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i64]
+    L.zro_gather_cast_bf16.restype = ctypes.c_int
+    L.zro_gather_cast_bf16.argtypes = [_i32, _i64, _i64, _vp, _vp]
+    L.zro_rs_adam_fused.restype = ctypes.c_int
+    L.zro_rs_adam_fused.argtypes = [_i32, _i64, _i64, _i64, _i64, _vp, _i32, _f32,
+                                    _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i64,
+                                    _vp, _vp]
+    L.zro_comm_bytes.restype = ctypes.c_int
+    L.zro_comm_bytes.argtypes = [_i32, _i32, _i64, _i32, ctypes.POINTER(ctypes.c_double)]
+    L.zro_layout_bytes.restype = ctypes.c_int
+    L.zro_layout_bytes.argtypes = [_i32, _i64, _i64, ctypes.POINTER(ctypes.c_double)]
+    L.zro_bf16_to_f32.restype = None
+    L.zro_bf16_to_f32.argtypes = [_vp, _vp, _i64]
+    L.zro_f32_to_bf16.restype = None
+    L.zro_f32_to_bf16.argtypes = [_vp, _vp, _i64]
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise OracleError(f"{what} returned {rc}")
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _ptr_array(arrs: Sequence[np.ndarray]):
+    return (ctypes.c_void_p * len(arrs))(*[_ptr(a) for a in arrs])
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float32:
+        return FP32
+    raise TypeError(f"oracle takes bf16 bit patterns (uint16) or float32, got {a.dtype}")
+
+
+# ----------------------------------------------------------------------------
+# Layout
+# ----------------------------------------------------------------------------
+
+@dataclass
+class Layout:
+    numel: np.ndarray          # [n] int64
+    world: int
+    bucket_size: int
+    T: int
+    P: int
+    S: int
+    offset: np.ndarray         # [n]
+    bucket_of: np.ndarray      # [n]
+    bucket_range: np.ndarray   # [nb, 2] flat [start, end)
+    slices: np.ndarray         # [ns, 7] param, bucket, dst, param_offset, bucket_offset, partition_offset, numel
+    runs: np.ndarray           # [nr, 5] bucket, dst, bucket_offset, partition_offset, numel
+
+    @property
+    def n_params(self) -> int:
+        return int(self.numel.shape[0])
+
+    @property
+    def n_buckets(self) -> int:
+        return int(self.bucket_range.shape[0])
+
+    def bucket(self, b: int):
+        s, e = (int(x) for x in self.bucket_range[b])
+        return s, e - s
+
+    def param_partitions(self, i: int):
+        """(param_to_partition_ids, grad_start_offset) of param i."""
+        rows = self.slices[self.slices[:, 0] == i]
+        return [int(r) for r in rows[:, 2]], [int(g) for g in rows[:, 3]]
+
+    def runs_of(self, b: int) -> np.ndarray:
+        return self.runs[self.runs[:, 0] == b]
+
+
+def layout(numel: Sequence[int], world: int, bucket_size: int) -> Layout:
+    L = lib()
+    nm = np.ascontiguousarray(np.asarray(numel, dtype=np.int64))
+    n = int(nm.shape[0])
+    dims = np.zeros(6, dtype=np.int64)
+    _check(L.zro_layout(_ptr(nm) if n else None, n, world, bucket_size, _ptr(dims),
+                        None, None, None, None, None), "zro_layout(count)")
+    T, P, S, nb, ns, nr = (int(x) for x in dims)
+    offset = np.zeros(max(n, 1), dtype=np.int64)
+    bucket_of = np.zeros(max(n, 1), dtype=np.int64)
+    br = np.zeros((max(nb, 1), 2), dtype=np.int64)
+    sl = np.zeros((max(ns, 1), 7), dtype=np.int64)
+    ru = np.zeros((max(nr, 1), 5), dtype=np.int64)
+    _check(L.zro_layout(_ptr(nm) if n else None, n, world, bucket_size, _ptr(dims),
+                        _ptr(offset), _ptr(bucket_of), _ptr(br), _ptr(sl), _ptr(ru)),
+           "zro_layout(fill)")
+    return Layout(nm, world, bucket_size, T, P, S, offset[:n], bucket_of[:n], br[:nb],
+                  sl[:ns], ru[:nr])
+
+
+# ----------------------------------------------------------------------------
+# Numerics
+# ----------------------------------------------------------------------------
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float32)
+    lib().zro_bf16_to_f32(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().zro_f32_to_bf16(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def bucket_pack(lay: Layout, b: int, grads: Sequence[Sequence[np.ndarray]]) -> List[np.ndarray]:
+    """grads[k][i]: replica k's grad of param i (uint16 bf16 bits or float32)."""
+    start, nb = lay.bucket(b)
+    end = start + nb
+    dt = grads[0][0].dtype
+    es = np.dtype(dt).itemsize
+    out = [np.empty(nb, dtype=dt) for _ in range(lay.world)]
+    n = lay.n_params
+    flat = []
+    for k in range(lay.world):
+        for i in range(n):
+            a = grads[k][i]
+            assert a.dtype == dt and a.shape == (int(lay.numel[i]),)
+            flat.append(np.ascontiguousarray(a))
+    ptrs = _ptr_array(flat)
+    _check(lib().zro_bucket_pack(_ptr(lay.numel), _ptr(lay.offset), n, lay.world, lay.T,
+                                 start, end, ptrs, es, _ptr_array(out)), "zro_bucket_pack")
+    return out
+
+
+def reduce_scatter_avg(lay: Layout, b: int, bucket: Sequence[np.ndarray], scale: float,
+                       shards: Sequence[np.ndarray]) -> None:
+    """Writes the averaged bucket into shards[r] (float32 [S]) in place."""
+    start, nb = lay.bucket(b)
+    code = _dtype_code(bucket[0])
+    for s in shards:
+        assert s.dtype == np.float32 and s.shape == (lay.S,)
+    _check(lib().zro_reduce_scatter_avg(lay.world, lay.S, start, nb, _ptr_array(bucket), code,
+                                        scale, _ptr_array(shards)), "zro_reduce_scatter_avg")
+
+
+def allreduce_avg(world: int, bucket: Sequence[np.ndarray], scale: float) -> List[np.ndarray]:
+    nb = int(bucket[0].shape[0])
+    code = _dtype_code(bucket[0])
+    out = [np.empty(nb, dtype=np.float32) for _ in range(world)]
+    _check(lib().zro_allreduce_avg(world, nb, _ptr_array(bucket), code, scale, _ptr_array(out)),
+           "zro_allreduce_avg")
+    return out
+
+
+def grad_accumulate(main_grad: np.ndarray, g: np.ndarray) -> None:
+    assert main_grad.dtype == np.float32 and main_grad.shape == g.shape
+    _check(lib().zro_grad_accumulate(main_grad.size, _ptr(main_grad), _ptr(g), _dtype_code(g)),
+           "zro_grad_accumulate")
+
+
+def adamw_scalars(hp) -> np.ndarray:
+    out = np.zeros(8, dtype=np.float32)
+    _check(lib().zro_adamw_scalars(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay,
+                                   hp.step, _ptr(out)), "zro_adamw_scalars")
+    return out
+
+
+def adamw(p: np.ndarray, m: np.ndarray, v: np.ndarray, g: np.ndarray, hp) -> None:
+    """In-place AdamW step on float32 arrays; hp has lr, beta1, beta2, eps, weight_decay, step."""
+    for a in (p, m, v, g):
+        assert a.dtype == np.float32 and a.shape == p.shape
+    _check(lib().zro_adamw(p.size, _ptr(p), _ptr(m), _ptr(v), _ptr(g), hp.lr, hp.beta1,
+                           hp.beta2, hp.eps, hp.weight_decay, hp.step), "zro_adamw")
+
+
+def gather_cast_bf16(lay: Layout, master: Sequence[np.ndarray]) -> np.ndarray:
+    out = np.empty(lay.P, dtype=np.uint16)
+    _check(lib().zro_gather_cast_bf16(lay.world, lay.T, lay.S, _ptr_array(master), _ptr(out)),
+           "zro_gather_cast_bf16")
+    return out
+
+
+def rs_adam_fused(lay: Layout, b: int, bucket: Sequence[np.ndarray], scale: float,
+                  master, m, v, hp, param_bf16: Optional[np.ndarray] = None,
+                  grad_out: Optional[Sequence[np.ndarray]] = None) -> None:
+    start, nb = lay.bucket(b)
+    code = _dtype_code(bucket[0])
+    _check(lib().zro_rs_adam_fused(
+        lay.world, lay.T, lay.S, start, nb, _ptr_array(bucket), code, scale,
+        _ptr_array(master), _ptr_array(m), _ptr_array(v),
+        hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step,
+        None if param_bf16 is None else _ptr(param_bf16),
+        None if grad_out is None else _ptr_array(grad_out)), "zro_rs_adam_fused")
+
+
+def comm_bytes(scheme: int, world: int, S: int, elem_bytes: int) -> float:
+    out = ctypes.c_double()
+    _check(lib().zro_comm_bytes(scheme, world, S, elem_bytes, ctypes.byref(out)), "zro_comm_bytes")
+    return out.value
+
+
+def layout_bytes(stage: int, T: int, S: int) -> float:
+    out = ctypes.c_double()
+    _check(lib().zro_layout_bytes(stage, T, S, ctypes.byref(out)), "zro_layout_bytes")
+    return out.value
+
+
+# ----------------------------------------------------------------------------
+# Convenience: whole-flat-space helpers used by tests and the CPU baseline
+# ----------------------------------------------------------------------------
+
+def shards_from_flat(lay: Layout, flat: np.ndarray) -> List[np.ndarray]:
+    """Split a flat float32 [T] array into N partition arrays of S, zero padded."""
+    full = np.zeros(lay.P, dtype=np.float32)
+    full[: lay.T] = flat[: lay.T]
+    return [np.ascontiguousarray(full[r * lay.S:(r + 1) * lay.S]) for r in range(lay.world)]
+
+
+def params_from_flat(lay: Layout, flat: np.ndarray) -> List[np.ndarray]:
+    """Views of a flat [T] array as the per-parameter tensors."""
+    return [flat[int(o): int(o) + int(n)] for o, n in zip(lay.offset, lay.numel)]
