@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark: params/s through the partition-aware ZeRO step on one GB300.
+
+One step is the whole hot path for every bucket, in order: IPG packing of each
+emulated rank's per-parameter bf16 gradients into its bucket, then the fused
+reduce-scatter (1/N predivide) + AdamW + bf16 cast. Default workload: the
+irregular layout (10,000 log-uniform params, 718,175,492 elements, 16 emulated
+ranks, 2^24-element buckets, integer-valued grads), each rank's gradients laid
+out as separately allocated tensors (512-byte aligned starts). Inputs are
+synthetic, drawn on the device; every bucket's working set (~1 GB) exceeds
+L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on
+the host instead (a bounded sample of the same workload per step).
+Under torchrun each rank runs its own copy of the workload on its own GPU
+("replicas only": the emulated data-parallel group lives on one GPU and
+nothing crosses GPUs); only a host-side gloo barrier and max are used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "params/s through fused reduce-scatter+AdamW shard step; HBM GB/s vs peak"
+UNIT = "params/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="zr", choices=["zr", "reference"])
+    ap.add_argument("--workload", default="irregular_10k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Dist:
+    """Host-side barrier / max over ranks (gloo); no data-path collective."""
+
+    def __init__(self, world):
+        self.world = world
+        self.pg = None
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("zero_partition_aware_gb300/csrc/kernels.cu", "zero_partition_aware_gb300/csrc/zr_internal.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def build_state(wl, device):
+    import torch
+    from zero_partition_aware_gb300 import workloads as W
+    from zero_partition_aware_gb300.engine import DPGroup
+    grp = DPGroup(list(wl.numel), wl.world, wl.bucket, device=device)
+    gen = W.generator(device, 0)
+    T = wl.total
+    master = torch.randn(T, generator=gen, device=device).mul_(wl.master_std)
+    # each rank's grads: per-parameter tensors at 512-byte aligned starts of one arena
+    offs = W.arena_offsets(wl.numel, 256)
+    arena_n = offs[-1] + wl.numel[-1]
+    arenas = [W.draw_grad(wl, arena_n, gen, device) for _ in range(wl.world)]
+    m = W.draw_state(wl, T, gen, device)
+    v = W.draw_state(wl, T, gen, device)
+    grp.load_flat(master, m, v)
+    del master, m, v
+    views = [[a[o:o + n] for o, n in zip(offs, wl.numel)] for a in arenas]
+    table = grp.grad_table(views)
+    return grp, arenas, table, offs
+
+
+def bucket_bytes(grp, b, world):
+    """Algorithmic bytes of the pack and of the fused kernel for bucket b."""
+    L = grp.layout
+    start, nb = L.bucket(b)
+    real = max(0, min(start + nb, L.T) - start)  # elements that come from parameter grads
+    pack = world * (2 * real + 2 * nb)            # read real grads, write the whole bucket
+    fused = nb * (2 * world + 12 + 12 + 2)        # N bf16 grads + p,m,v read + p,m,v write + bf16 param
+    return pack, fused
+
+
+def run_gpu(args, rank, nranks, local, dist):
+    import torch
+    from zero_partition_aware_gb300 import workloads as W
+    from zero_partition_aware_gb300 import zr
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    wl = W.WORKLOADS[args.workload]
+    grp, arenas, table, offs = build_state(wl, device)
+    L = grp.layout
+    hp = W.AdamW(step=wl.adam.step)
+    nbk = L.n_buckets
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    pack_b, fused_b = zip(*[bucket_bytes(grp, b, wl.world) for b in range(nbk)])
+    pack_bytes, fused_bytes = sum(pack_b), sum(fused_b)
+
+    def step(evs=None):
+        for b in range(nbk):
+            if evs is not None:
+                evs[2 * b].record(stream)
+            grp.pack(b, table, stream)
+            if evs is not None:
+                evs[2 * b + 1].record(stream)
+            grp.fused(b, hp, stream=stream)
+        if evs is not None:
+            evs[2 * nbk].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, events around every pack and every fused launch group
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nbk + 1)] for _ in range(args.steps)]
+    start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    n0 = zr.zr_launch_count()
+    start_ev.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    end_ev.record(stream)
+    torch.cuda.synchronize()
+    launches = zr.zr_launch_count() - n0
+    dist.barrier()
+    clk = clocks.stop()
+    total_ms = start_ev.elapsed_time(end_ev)
+    t_pack = sum(evs[k][2 * b].elapsed_time(evs[k][2 * b + 1]) for k in range(args.steps) for b in range(nbk))
+    t_fused = sum(evs[k][2 * b + 1].elapsed_time(evs[k][2 * b + 2]) for k in range(args.steps) for b in range(nbk))
+    ms_step = dist.max(total_ms / args.steps)
+    value = nranks * L.T / (ms_step / 1e3)
+
+    peak, peak_kind = measured_peaks()
+    fused_gbs = fused_bytes * args.steps / (t_fused / 1e3) / 1e9
+    pack_gbs = pack_bytes * args.steps / (t_pack / 1e3) / 1e9
+    dominant = "fused" if t_fused >= t_pack else "pack"
+    if dominant == "fused":
+        ach, per_launch, kname = fused_gbs, fused_bytes / nbk, "rs_adam_fused_bf16_w16"
+    else:
+        ach, per_launch, kname = pack_gbs, pack_bytes / nbk, "bucket_pack_bf16"
+    tr = profiled_traffic(kname)
+    roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "kernel": kname, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": round(per_launch)}
+    kernels = {
+        "rs_adam_fused": {"ms_per_step": round(t_fused / args.steps, 4), "GB_per_s": round(fused_gbs, 1),
+                          "frac_of_peak": round(fused_gbs / peak, 4), "params_per_s": round(
+                              L.P / (t_fused / args.steps / 1e3)), "bytes_per_param": 2 * wl.world + 26},
+        "bucket_pack": {"ms_per_step": round(t_pack / args.steps, 4), "GB_per_s": round(pack_gbs, 1),
+                        "frac_of_peak": round(pack_gbs / peak, 4), "bytes_per_param": 4 * wl.world},
+        "time_share": {"rs_adam_fused": round(t_fused / (t_fused + t_pack), 4),
+                       "bucket_pack": round(t_pack / (t_fused + t_pack), 4)},
+    }
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, grp, arenas, table, hp, stream, nranks, dist)
+
+    out = {"metric": METRIC, "value": round(value), "unit": UNIT, "n_gpus": nranks, "steps": args.steps,
+           "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": wl.name, "params": L.T, "padded": L.P, "world": wl.world,
+                      "reduce_bucket_size": wl.bucket, "buckets": nbk, "grad_dtype": "bf16",
+                      "grad_layout": "per-parameter tensors, 512-byte aligned starts",
+                      "step": "per bucket: zr_bucket_pack + zr_rs_adam_fused",
+                      "l2": "no flush: every bucket's working set (~1 GB) exceeds the 129 MB L2",
+                      "parallelism": f"replicas only x{nranks}"},
+           "roofline": roofline, "kernels": kernels, "gpu_launches": int(launches), "clocks": clk}
+    if e2e is not None:
+        out["e2e"] = e2e
+    return out
+
+
+def run_e2e(args, grp, arenas, table, hp, stream, nranks, dist):
+    """The same step through the public API with the gradients starting in pinned
+    host memory: per step, H2D of every rank's gradients, the step, D2H of the
+    full bf16 parameter buffer."""
+    import torch
+    L = grp.layout
+    try:
+        host = [torch.empty(a.numel(), dtype=a.dtype, pin_memory=True) for a in arenas]
+    except RuntimeError as e:
+        return {"value": None, "unit": UNIT, "error": f"pinned host allocation failed: {e}"}
+    for h, a in zip(host, arenas):
+        h.copy_(a)
+    out_host = torch.empty(L.P, dtype=torch.bfloat16, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for a, h in zip(arenas, host):
+            a.copy_(h, non_blocking=True)
+        for b in range(L.n_buckets):
+            grp.pack(b, table, stream)
+            grp.fused(b, hp, stream=stream)
+        out_host.copy_(grp.param[: L.P], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    k = max(2, min(args.steps, 5))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    s.record(stream)
+    for _ in range(k):
+        e2e_step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(s.elapsed_time(e) / k)
+    del host
+    return {"value": round(nranks * L.T / (ms / 1e3)), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": k}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and --impl reference)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(wl, n_elems, seed=0):
+    """A bounded sample of the workload on the host: the first bucket's leading
+    params (at most n_elems elements) with their state, drawn on the CPU."""
+    import torch
+    import oracle
+    from zero_partition_aware_gb300 import workloads as W
+    numel = []
+    tot = 0
+    for n in wl.numel:
+        if tot + n > n_elems and numel:
+            break
+        numel.append(int(n))
+        tot += int(n)
+    sub = W.replace(wl, numel=tuple(numel))
+    lay = oracle.layout(numel, wl.world, wl.bucket)
+    inp = W.draw_inputs(sub, "cpu", seed=seed)
+    grads = [oracle.params_from_flat(lay, W.bf16_bits(inp["grads"][k][0])) for k in range(wl.world)]
+    p = oracle.shards_from_flat(lay, inp["master"].numpy())
+    m = oracle.shards_from_flat(lay, inp["m"].numpy())
+    v = oracle.shards_from_flat(lay, inp["v"].numpy())
+    return lay, grads, p, m, v
+
+
+def oracle_step(lay, grads, p, m, v, hp, scale):
+    import oracle
+    param = np.zeros(lay.P, np.uint16)
+    for b in range(lay.n_buckets):
+        bucket = oracle.bucket_pack(lay, b, grads)
+        oracle.rs_adam_fused(lay, b, bucket, scale, p, m, v, hp, param)
+    return param
+
+
+def cpu_baseline(wl, budget_s):
+    """Time the oracle as it stands, single-threaded, on a sample sized to ~budget_s."""
+    import oracle
+    oracle.build()
+    scale = float(np.float32(1.0 / wl.world))
+    hp = wl.adam
+    # calibrate on a small sample, then size the timed sample to the budget
+    lay, grads, p, m, v = oracle_sample(wl, 200_000)
+    t0 = time.perf_counter()
+    oracle_step(lay, grads, p, m, v, hp, scale)
+    rate = lay.T / max(time.perf_counter() - t0, 1e-6)
+    n = int(min(max(rate * budget_s, 200_000), 1 << 24))
+    lay, grads, p, m, v = oracle_sample(wl, n)
+    t0 = time.perf_counter()
+    oracle_step(lay, grads, p, m, v, hp, scale)
+    dt = time.perf_counter() - t0
+    return {"value": round(lay.T / dt), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {lay.n_params} params ({lay.T} elements) of {wl.name}, world {wl.world}: "
+                      f"pack + fused step, {dt:.1f} s single-threaded",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    from zero_partition_aware_gb300 import workloads as W
+    import oracle
+    wl = W.WORKLOADS[args.workload]
+    oracle.build()
+    scale = float(np.float32(1.0 / wl.world))
+    # each step: a bounded sample (~2 s of single-threaded oracle work)
+    lay, grads, p, m, v = oracle_sample(wl, 200_000)
+    t0 = time.perf_counter()
+    oracle_step(lay, grads, p, m, v, wl.adam, scale)
+    rate = lay.T / max(time.perf_counter() - t0, 1e-6)
+    per_step = max(2.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
+    lay, grads, p, m, v = oracle_sample(wl, int(min(max(rate * per_step, 200_000), 1 << 24)))
+    for _ in range(args.warmup):
+        oracle_step(lay, grads, p, m, v, wl.adam, scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(lay, grads, p, m, v, wl.adam, scale)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = lay.T / dt
+    sample = (f"first {lay.n_params} params ({lay.T} elements) of {wl.name}, world {wl.world}: "
+              f"pack + fused step per timed step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value), "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "params": lay.T, "world": wl.world,
+                       "reduce_bucket_size": wl.bucket, "sample_of_params": wl.total},
+            "cpu_baseline": {"value": round(value), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, nranks, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    from zero_partition_aware_gb300 import build
+    dist = Dist(nranks)
+    if rank == 0:
+        build.build()
+    dist.barrier()
+    out = run_gpu(args, rank, nranks, local, dist)
+    if rank == 0:
+        if nranks == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(W_lookup(args.workload), args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    dist.close()
+    return 0
+
+
+def W_lookup(name):
+    from zero_partition_aware_gb300 import workloads as W
+    return W.WORKLOADS[name]
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,278 @@
+/*
+ * zr.h -- C ABI of libzr: partition-aware ZeRO stage-1/2 gradient averaging
+ * followed by the sharded AdamW step, on one GPU (sm_103a).
+ *
+ * The data-parallel group of N ranks is emulated on one device: each rank's
+ * gradients, bucket and optimizer shard are separate device buffers, and the
+ * collectives become local HBM reductions over those N buffers. Nothing
+ * crosses GPUs; the library issues no collective and links no communication
+ * library.
+ *
+ * Sources, cited by page title and section:
+ *   [DS] "DeepSpeed ZeRO 通信优化深度解析：用 reduce-scatter 分区感知规约替代 all-reduce"
+ *   [MG] "Megatron-LM 分布式训练（四）：数据并行 DP 与分布式优化器（ZeRO）"
+ *   [IQ] "07. 大规模训练时通信瓶颈在哪里？AllReduce、AllGather、ReduceScatter 有什么区别？"
+ *
+ * Notation: N = world, n_i = numel of param i, o_i = sum_{j<i} n_j,
+ * T = sum n_i, P = ceil(T/N)*N (tail padding only), S = P/N; rank r owns the
+ * flat range [rS, (r+1)S).
+ *
+ * Conventions for every entry point:
+ *  - Returns ZR_OK (0) or a negative ZR_ERR_* status; zr_last_error() gives
+ *    a message for the calling thread's last failure. The library never
+ *    throws across this boundary, never exits or aborts, and its kernels
+ *    never trap.
+ *  - Device buffers are owned by the caller. The library allocates only the
+ *    host-side layout handle (freed by zr_layout_destroy); its kernels use no
+ *    scratch memory and take their tables as launch parameters.
+ *  - "host array of device pointers": a host array (read during the call
+ *    only) whose entries are device addresses.
+ *  - Kernels are enqueued on `stream` (NULL = the legacy default stream) and
+ *    the call returns without synchronising. Launch errors are reported;
+ *    errors of the asynchronous execution surface at the caller's next
+ *    synchronisation.
+ *  - Device pointers need only element alignment (2 bytes for bf16, 4 for
+ *    fp32); otherwise ZR_ERR_ALIGN. Any 16-byte phase is accepted.
+ *  - Outputs must not overlap inputs except where an argument is in/out.
+ */
+#ifndef ZR_H
+#define ZR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZR_OK 0
+#define ZR_ERR_INVALID_ARG (-1)  /* NULL, out-of-range index, bad size or dtype */
+#define ZR_ERR_CUDA (-2)         /* a CUDA runtime call or launch failed */
+#define ZR_ERR_OOM (-3)          /* host allocation failed */
+#define ZR_ERR_ALIGN (-4)        /* a device pointer is not element-aligned */
+#define ZR_ERR_TIMEOUT (-5)      /* reserved: a bounded device wait ran out */
+#define ZR_ERR_STATE (-6)        /* no usable CUDA device / wrong device state */
+#define ZR_ERR_UNSUPPORTED (-7)  /* a size beyond what this build supports */
+
+/* Largest world (emulated data-parallel size) the kernels accept. */
+#define ZR_MAX_WORLD 1024
+
+/* Defaults of the zero_optimization keys ([DS] §五 table). */
+#define ZR_DEFAULT_REDUCE_BUCKET_SIZE 500000000LL
+#define ZR_DEFAULT_REDUCE_SCATTER 1
+#define ZR_DEFAULT_CONTIGUOUS_GRADIENTS 1
+#define ZR_DEFAULT_OVERLAP_COMM 0
+
+typedef struct CUstream_st *zr_stream; /* the same type as cudaStream_t */
+typedef struct zr_layout zr_layout;    /* opaque, host-owned */
+
+typedef enum { ZR_BF16 = 0, ZR_FP32 = 1 } zr_dtype;
+
+typedef struct {
+    int64_t T, P, S;               /* total, padded total, partition size */
+    int64_t n_params, n_buckets, n_slices, n_runs;
+    int64_t reduce_bucket_size;
+    int32_t world;
+} zr_layout_info;
+
+/* One (param, partition) intersection ([DS] §三.2: a param's grad cut by
+ * destination partition into (dst_rank, bucket_offset, numel) pieces). */
+typedef struct {
+    int64_t param, bucket;
+    int32_t dst;
+    int64_t param_offset;      /* grad_start_offset: offset inside the param's grad */
+    int64_t bucket_offset;     /* offset inside the bucket */
+    int64_t partition_offset;  /* offset inside rank dst's partition */
+    int64_t numel;
+} zr_slice;
+
+/* Slices of one bucket aimed at one rank, merged ([DS] §三.2: contiguous
+ * fragments for the same target are reduced together); the tail padding is
+ * part of the last bucket's runs. */
+typedef struct {
+    int64_t bucket;
+    int32_t dst;
+    int64_t bucket_offset, partition_offset, numel;
+} zr_run;
+
+/* AdamW hyper-parameters; step is the 1-based step count t. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+} zr_adamw;
+
+/* The fp32 scalars one AdamW step uses, each computed on the host in double
+ * from the fp32 hyper-parameters and rounded once. */
+typedef struct {
+    float beta1, one_minus_beta1, beta2, one_minus_beta2;
+    float step_size;  /* lr / (1 - beta1^t) */
+    float bc2_sqrt;   /* sqrt(1 - beta2^t) */
+    float decay;      /* 1 - lr * weight_decay */
+    float eps;
+} zr_adamw_scalars;
+
+/* ---- status ------------------------------------------------------------ */
+
+const char *zr_status_string(int status);
+/* Copies the calling thread's last error message (NUL-terminated, truncated
+ * to cap). Returns the full message length. */
+int zr_last_error(char *buf, size_t cap);
+int zr_version(void);
+/* Number of kernels this process has launched through libzr so far (all
+ * threads, all devices); lets a caller count the launches of a region. */
+int64_t zr_launch_count(void);
+
+/* ---- layout (host only) ------------------------------------------------ */
+
+/*
+ * Builds the flat partitioned layout of n_params parameters of numel[i] >= 1
+ * elements each, for `world` ranks (1..ZR_MAX_WORLD), with buckets of at most
+ * reduce_bucket_size >= 1 elements.
+ *  - Flat layout: params concatenated in order, padded at the tail to a
+ *    multiple of world, split in world equal partitions ([DS] §二; [MG]
+ *    §"分布式优化器": each card keeps 1/DP of the optimizer state).
+ *  - Buckets: params in ascending order; a bucket is closed before a param
+ *    that would overflow it, so an oversized param sits alone; the last
+ *    bucket also covers the padding [T, P) ([DS] §四, reduce_bucket_size; §五).
+ * n_params = 0 gives an empty layout (T = P = S = 0, no buckets).
+ * *out is owned by the caller and freed with zr_layout_destroy.
+ */
+int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
+                     int64_t reduce_bucket_size, zr_layout **out);
+int zr_layout_destroy(zr_layout *layout);
+int zr_layout_query(const zr_layout *layout, zr_layout_info *info);
+
+/* param_to_partition_ids and grad_start_offset of one param ([DS] §三.2).
+ * Writes min(cap, count) entries (either array may be NULL) and the count. */
+int zr_layout_param_partitions(const zr_layout *layout, int64_t param, int32_t *part_ids,
+                               int64_t *grad_start_offset, int32_t cap, int32_t *n_out);
+/* All slices (param order, then dst) / runs (bucket order, then dst). Writes
+ * min(cap, count) entries (out may be NULL to query the count). */
+int zr_layout_slices(const zr_layout *layout, zr_slice *out, int64_t cap, int64_t *n_out);
+int zr_layout_runs(const zr_layout *layout, zr_run *out, int64_t cap, int64_t *n_out);
+/* Flat start and element count of bucket b. */
+int zr_layout_bucket(const zr_layout *layout, int64_t b, int64_t *flat_start, int64_t *numel);
+/* Flat offset o_i of param i and the bucket it belongs to. */
+int zr_layout_param(const zr_layout *layout, int64_t param, int64_t *flat_offset, int64_t *bucket);
+
+/* ---- device steps ------------------------------------------------------ */
+
+/*
+ * IPG bucket packing ([DS] §四: each param's grad is copied into the
+ * contiguous reduce_bucket_size bucket; §五 contiguous_gradients).
+ * grads: host array [world * n_params] of device pointers, entry k*n_params+i
+ *   = replica k's grad of param i (numel[i] elements of dtype); only the
+ *   params of `bucket` are read (others may be NULL).
+ * bucket_out: host array [world] of device pointers, each receiving numel_b
+ *   elements: param i's element e at offset o_i - bucket_start + e, and zeros
+ *   at positions past T (the padding of the last bucket).
+ */
+int zr_bucket_pack(const zr_layout *layout, int64_t bucket, const void *const *grads,
+                   zr_dtype dtype, void *const *bucket_out, zr_stream stream);
+
+/*
+ * fp32 main-grad accumulation ([MG] §"四步接力" step 2: main_grad.add_(grad)
+ * into the fp32 contiguous buffer): main_grad[e] += float(g[e]), e < n.
+ * main_grad: device fp32 [n], in/out. g: device [n] of g_dtype.
+ */
+int zr_grad_accumulate(float *main_grad, const void *g, zr_dtype g_dtype, int64_t n,
+                       zr_stream stream);
+
+/*
+ * Reduce-scatter with average over one bucket ([DS] §三.2 and §六: predivide
+ * by the data-parallel size, then reduce each slice to its owner; [IQ]
+ * §"三种原语": GPU i gets segment i of the sum; [DS] §三.3
+ * copy_grads_in_partition).
+ * For every bucket position e (flat f = bucket_start + e, owner r = f / S):
+ *   shard_grad[r][f - rS] = sum over k = 0..world-1, in that order, of
+ *                           fp32(bucket_in[k][e]) * scale, summed in fp32.
+ * bucket_in: host array [world] of device pointers, numel_b elements each.
+ * scale: the predivide factor, normally 1/world (dp_world_size/sp_size per
+ *   [DS] §六); any finite value.
+ * shard_grad: host array [world] of device pointers, S fp32 each; only the
+ *   entries of ranks the bucket intersects are read, only positions inside
+ *   the bucket are written.
+ */
+int zr_reduce_scatter_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
+                          zr_dtype dtype, float scale, float *const *shard_grad, zr_stream stream);
+
+/*
+ * AdamW over whole partitions ([MG] §"通信模式": each card updates its own
+ * 1/DP slice with the fp32 master; §"朴素 DP 的致命浪费": master, m, v are
+ * the 12 sharded bytes). Per element, each operation rounded to fp32:
+ *   m' = b1 m + (1-b1) g;  v' = b2 v + (1-b2) g^2;
+ *   p' = p (1 - lr wd) - (lr/(1-b1^t)) * m' / (sqrt(v')/sqrt(1-b2^t) + eps).
+ * master, m, v (in/out) and grad: host arrays [world] of device pointers, S
+ * fp32 each. rank in [0, world) updates that rank's shard only (other
+ * entries may be NULL); rank = -1 updates every rank.
+ */
+int zr_adam_shard_step(const zr_layout *layout, int32_t rank, float *const *master,
+                       float *const *m, float *const *v, const float *const *grad,
+                       const zr_adamw *hp, zr_stream stream);
+
+/*
+ * All-gather payload ([MG] §"通信模式": the updated slices are concatenated
+ * back into the full weights for the next forward; [IQ] §"三种原语"):
+ *   param_bf16[f] = bf16_round_nearest_even(master[f / S][f % S]) for f < T,
+ *   param_bf16[f] = 0 for T <= f < P.
+ * master: host array [world] of device pointers, S fp32 each.
+ * param_bf16: device [P] bf16.
+ */
+int zr_gather_cast_bf16(const zr_layout *layout, const float *const *master, void *param_bf16,
+                        zr_stream stream);
+
+/*
+ * The three steps above in one pass over one bucket: the averaged gradient
+ * of each position is kept in registers, AdamW updates the owner's master,
+ * m and v, and the updated master is cast to bf16 into the full parameter
+ * buffer ([MG] §"通信模式": reduce-scatter, then the local fp32 update,
+ * then the all-gather's payload). Results are bit-identical to
+ * zr_reduce_scatter_avg + zr_adam_shard_step + zr_gather_cast_bf16 restricted
+ * to the bucket's positions.
+ * param_bf16: device [P] bf16 or NULL (not written).
+ * shard_grad_out: host array [world] of device pointers (S fp32 each) or NULL;
+ *   if given, it also receives the averaged gradient.
+ */
+int zr_rs_adam_fused(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
+                     zr_dtype dtype, float scale, float *const *master, float *const *m,
+                     float *const *v, const zr_adamw *hp, void *param_bf16,
+                     float *const *shard_grad_out, zr_stream stream);
+
+/*
+ * All-reduce with average over one bucket, the path used when
+ * reduce_scatter is off ([DS] §三.2 gradient_reduction_w_predivide; [MG]
+ * §"四步接力" step 4; [IQ] §"三种原语"): out[k][e] = the same averaged value
+ * as zr_reduce_scatter_avg, for every replica k.
+ * out: host array [world] of device pointers, numel_b fp32 each.
+ */
+int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
+                     zr_dtype dtype, float scale, float *const *out, zr_stream stream);
+
+/* ---- accounting (host only) -------------------------------------------- */
+
+/* The AdamW scalars the kernels use for `hp` (see zr_adamw_scalars). */
+int zr_adamw_prepare(const zr_adamw *hp, zr_adamw_scalars *out);
+
+/*
+ * Bytes one rank sends per step over the padded flat buffer, ring
+ * collectives ([MG] §"NCCL 底层算法": 2(N-1)/N of the message per card for a
+ * ring all-reduce; [DS] §一: 1.5x -> 1.0x of data parallelism):
+ *   scheme 0 DP all-reduce 2(N-1)S e; 1 first ZeRO-1 (all-reduce + all-gather)
+ *   3(N-1)S e; 2 partition-aware (reduce-scatter + all-gather) 2(N-1)S e;
+ *   3 reduce-scatter only (N-1)S e.
+ */
+int zr_comm_bytes(const zr_layout *layout, int32_t scheme, int32_t elem_bytes,
+                  double *per_rank_bytes);
+
+/*
+ * Per-rank bytes of weights, grads and optimizer state ([MG] §"朴素 DP 的致命
+ * 浪费": 2+2+4+4+4 = 16 per param; §"ZeRO 各档" table): stage 0 16T;
+ * stage 1 4T + 12S; stage 15 (ZeRO-1.5 / stage 2) 2T + 14S; stage 3 16S.
+ */
+int zr_layout_bytes(const zr_layout *layout, int32_t stage, double *bytes_per_rank);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZR_H */

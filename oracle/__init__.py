@@ -29,10 +29,22 @@ BF16, FP32 = 0, 1
 _lib = None
 
 
+def _foreign(path: str) -> bool:
+    """True if an ELF file was built for another machine (x86-64 vs aarch64)."""
+    import platform
+    want = {"x86_64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+        return want is not None and int.from_bytes(head[18:20], "little") != want
+    except OSError:
+        return True
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with the host C compiler (no FMA contraction)."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or \
+    if force or not os.path.exists(_LIB_PATH) or _foreign(_LIB_PATH) or \
             os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
         cc = os.environ.get("CC", "gcc")

@@ -1,0 +1,182 @@
+"""Host-side checks of libzr (CPU only, no kernel launches).
+
+The library loads, exports every entry point include/zr.h declares, and its
+host code -- layout, slices, runs, AdamW scalars, byte accounting -- agrees
+bit-exactly with the oracle. Argument errors come back as status codes.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from zero_partition_aware_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def zr():
+    from zero_partition_aware_gb300 import build
+    build.build()
+    from zero_partition_aware_gb300 import zr as mod
+    return mod
+
+
+def _declared_entry_points():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(zr_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol(zr):
+    declared = _declared_entry_points()
+    assert declared, "no declarations found"
+    lib = ctypes.CDLL(zr.LIB_PATH)
+    missing = [n for n in sorted(declared) if not hasattr(lib, n)]
+    assert not missing, missing
+    assert declared == set(zr.EXPORTED)
+
+
+def test_status_strings(zr):
+    assert zr.zr_status_string(0) == "ZR_OK"
+    assert zr.zr_status_string(-4) == "ZR_ERR_ALIGN"
+    assert zr.zr_version() >= 1
+
+
+def _same_layout(lib_lay, orc):
+    assert (lib_lay.T, lib_lay.P, lib_lay.S) == (orc.T, orc.P, orc.S)
+    assert lib_lay.n_buckets == orc.n_buckets
+    assert np.array_equal(lib_lay.slices(), orc.slices)
+    assert np.array_equal(lib_lay.runs(), orc.runs)
+    for b in range(orc.n_buckets):
+        assert lib_lay.bucket(b) == orc.bucket(b)
+    for i in range(orc.n_params):
+        assert lib_lay.param(i) == (int(orc.offset[i]), int(orc.bucket_of[i]))
+        assert lib_lay.param_partitions(i) == orc.param_partitions(i)
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_layout_matches_oracle_on_workloads(zr, name):
+    wl = W.WORKLOADS[name]
+    _same_layout(zr.Layout(list(wl.numel), wl.world, wl.bucket), oracle.layout(list(wl.numel), wl.world, wl.bucket))
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_layout_matches_oracle_random(zr, seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 40))
+    world = int(rng.choice([1, 2, 3, 5, 8, 16, 31, 64, 100]))
+    numel = W.random_numels(rng, n, 1, 5000)
+    B = int(rng.integers(1, 20000))
+    _same_layout(zr.Layout(numel, world, B), oracle.layout(numel, world, B))
+
+
+def test_layout_edges(zr):
+    for numel, world, B in [([1], 1, 1), ([1], 1024, 1), ([5, 1, 1, 1], 8, 2), ([3, 3, 3], 3, 3),
+                            ([10] * 7, 4, 1), ([7], 4, 1000)]:
+        _same_layout(zr.Layout(numel, world, B), oracle.layout(numel, world, B))
+    empty = zr.Layout([], 4, 10)
+    assert (empty.T, empty.P, empty.S, empty.n_buckets) == (0, 0, 0, 0)
+
+
+def test_layout_rejects_bad_arguments(zr):
+    for args in [([0], 2, 4), ([1, -3], 2, 4), ([4], 0, 4), ([4], 2, 0), ([4], zr.ZR_MAX_WORLD + 1, 4)]:
+        with pytest.raises(zr.ZrError) as ei:
+            zr.Layout(*args)
+        assert ei.value.status == zr.ZR_ERR_INVALID_ARG
+    lay = zr.Layout([10, 20], 2, 15)
+    with pytest.raises(zr.ZrError):
+        lay.bucket(5)
+    with pytest.raises(zr.ZrError):
+        lay.param(-1)
+
+
+def test_defaults_match_config_table(zr):
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "config_defaults.json")))
+    assert zr.ZR_DEFAULT_REDUCE_BUCKET_SIZE == g["reduce_bucket_size"]
+    assert zr.ZR_DEFAULT_REDUCE_SCATTER == g["reduce_scatter"]
+    assert zr.ZR_DEFAULT_CONTIGUOUS_GRADIENTS == g["contiguous_gradients"]
+    assert zr.ZR_DEFAULT_OVERLAP_COMM == g["overlap_comm"]
+    hdr = open(os.path.join(ROOT, "include", "zr.h")).read()
+    assert re.search(r"ZR_DEFAULT_REDUCE_BUCKET_SIZE\s+500000000LL", hdr)
+
+
+@pytest.mark.parametrize("step", [1, 2, 10, 1000, 100000])
+def test_adamw_scalars_match_oracle(zr, step):
+    hp = W.AdamW(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=step)
+    mine = zr.zr_adamw_prepare(hp)
+    ref = oracle.adamw_scalars(hp)
+    got = np.array([mine[k] for k in ("beta1", "one_minus_beta1", "beta2", "one_minus_beta2", "step_size",
+                                      "bc2_sqrt", "decay", "eps")], np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_adamw_scalars_reject_bad_hyperparameters(zr):
+    for hp in [W.AdamW(step=0), W.AdamW(beta1=1.0), W.AdamW(eps=0.0), W.AdamW(lr=float("nan"))]:
+        with pytest.raises(zr.ZrError):
+            zr.zr_adamw_prepare(hp)
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_accounting_matches_oracle(zr, name):
+    wl = W.WORKLOADS[name]
+    lay = zr.Layout(list(wl.numel), wl.world, wl.bucket)
+    for scheme in range(4):
+        for e in (2, 4):
+            assert zr.zr_comm_bytes(lay, scheme, e) == oracle.comm_bytes(scheme, wl.world, lay.S, e)
+    for stage in (0, 1, 15, 3):
+        assert zr.zr_layout_bytes(lay, stage) == oracle.layout_bytes(stage, lay.T, lay.S)
+    with pytest.raises(zr.ZrError):
+        zr.zr_comm_bytes(lay, 4, 2)
+    with pytest.raises(zr.ZrError):
+        zr.zr_layout_bytes(lay, 2)
+
+
+def test_device_steps_validate_before_launch(zr):
+    """NULL and misaligned pointers are rejected on the host; nothing is launched."""
+    lay = zr.Layout([100, 200], 2, 1000)
+    L = zr._lib
+    two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    odd = (ctypes.c_void_p * 2)(0x1001, 0x2000)
+    nul = (ctypes.c_void_p * 2)(0, 0x2000)
+    hp = zr.zr_adamw(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)
+    assert L.zr_reduce_scatter_avg(lay.handle, 0, nul, zr.ZR_BF16, 0.5, two, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_reduce_scatter_avg(lay.handle, 0, odd, zr.ZR_BF16, 0.5, two, None) == zr.ZR_ERR_ALIGN
+    assert L.zr_reduce_scatter_avg(lay.handle, 7, two, zr.ZR_BF16, 0.5, two, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_reduce_scatter_avg(lay.handle, 0, two, 9, 0.5, two, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_reduce_scatter_avg(lay.handle, 0, two, zr.ZR_BF16, float("inf"), two, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_rs_adam_fused(lay.handle, 0, two, zr.ZR_BF16, 0.5, two, two, two, None, None, None,
+                              None) == zr.ZR_ERR_INVALID_ARG
+    bad = zr.zr_adamw(1e-3, 0.9, 0.999, 1e-8, 0.01, 0)
+    assert L.zr_rs_adam_fused(lay.handle, 0, two, zr.ZR_BF16, 0.5, two, two, two, ctypes.byref(bad), None,
+                              None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_rs_adam_fused(lay.handle, 0, two, zr.ZR_BF16, 0.5, two, two, two, ctypes.byref(hp),
+                              ctypes.c_void_p(0x1001), None, None) == zr.ZR_ERR_ALIGN
+    assert L.zr_adam_shard_step(lay.handle, 2, two, two, two, two, ctypes.byref(hp), None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_gather_cast_bf16(lay.handle, two, ctypes.c_void_p(0x1001), None) == zr.ZR_ERR_ALIGN
+    assert L.zr_grad_accumulate(ctypes.c_void_p(0x1002), ctypes.c_void_p(0x2000), zr.ZR_BF16, 10,
+                                None) == zr.ZR_ERR_ALIGN
+    assert L.zr_grad_accumulate(None, None, zr.ZR_BF16, 0, None) == zr.ZR_OK  # empty: nothing to do
+    assert L.zr_grad_accumulate(None, None, zr.ZR_BF16, -1, None) == zr.ZR_ERR_INVALID_ARG
+    grads = (ctypes.c_void_p * 4)(0x1000, 0x2001, 0x3000, 0x4000)
+    assert L.zr_bucket_pack(lay.handle, 0, grads, zr.ZR_BF16, two, None) == zr.ZR_ERR_ALIGN
+    assert "grads" in zr.last_error()
+
+
+def test_launch_without_device_reports_state(zr):
+    """With no usable GPU a well-formed call fails with ZR_ERR_STATE (never run where a GPU exists)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: this check only runs on a machine without one")
+    lay = zr.Layout([100, 200], 2, 1000)
+    two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    rc = zr._lib.zr_reduce_scatter_avg(lay.handle, 0, two, zr.ZR_BF16, 0.5, two, None)
+    assert rc in (zr.ZR_ERR_STATE, zr.ZR_ERR_CUDA)

@@ -1,0 +1,99 @@
+"""An emulated data-parallel group on one GPU, driven through libzr's C ABI.
+
+``DPGroup`` owns what each of the N ranks would hold under ZeRO stage 1/2
+("Megatron-LM 分布式训练（四）" §"ZeRO 各档"; "DeepSpeed ZeRO 通信优化深度解析"
+§二, §三.3): its fp32 master, m and v partition of S elements, its IPG bucket
+buffer (reused bucket after bucket, as stage 2 releases it once the slice is
+reduced), and the full bf16 parameter buffer the all-gather refreshes. One
+``step`` runs, for every bucket in order, the packing of each rank's
+per-parameter gradients into its bucket and the fused reduce-scatter + AdamW
++ bf16 cast; nothing here computes, every step is a libzr kernel.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import zr
+
+
+class DPGroup:
+    def __init__(self, numel: Sequence[int], world: int,
+                 reduce_bucket_size: int = zr.ZR_DEFAULT_REDUCE_BUCKET_SIZE,
+                 grad_dtype: torch.dtype = torch.bfloat16, device: str = "cuda",
+                 allocate_buckets: bool = True):
+        self.layout = zr.Layout(numel, world, reduce_bucket_size)
+        self.world = world
+        self.device = torch.device(device)
+        self.grad_dtype = grad_dtype
+        self.zr_dtype = zr.ZR_BF16 if grad_dtype == torch.bfloat16 else zr.ZR_FP32
+        L = self.layout
+        S = L.S
+        f32 = dict(dtype=torch.float32, device=self.device)
+        self.master = [torch.zeros(S, **f32) for _ in range(world)]
+        self.m = [torch.zeros(S, **f32) for _ in range(world)]
+        self.v = [torch.zeros(S, **f32) for _ in range(world)]
+        self.param = torch.zeros(max(L.P, 1), dtype=torch.bfloat16, device=self.device)
+        self.max_bucket = max((L.bucket(b)[1] for b in range(L.n_buckets)), default=0)
+        self.buckets: List[torch.Tensor] = []
+        if allocate_buckets:
+            self.buckets = [torch.empty(max(self.max_bucket, 1), dtype=grad_dtype, device=self.device)
+                            for _ in range(world)]
+        self._p_master = zr.PtrArray(self.master)
+        self._p_m = zr.PtrArray(self.m)
+        self._p_v = zr.PtrArray(self.v)
+        self._p_buckets = zr.PtrArray(self.buckets) if self.buckets else None
+        self.scale = float(torch.tensor(1.0 / world, dtype=torch.float32).item())
+
+    # ---- state ------------------------------------------------------------------
+    def load_flat(self, master: torch.Tensor, m: Optional[torch.Tensor] = None,
+                  v: Optional[torch.Tensor] = None) -> None:
+        """Scatter flat [T] fp32 state into the N partitions (padding zero)."""
+        L = self.layout
+        for dst, src in ((self.master, master), (self.m, m), (self.v, v)):
+            if src is None:
+                continue
+            for r in range(self.world):
+                lo, hi = r * L.S, min((r + 1) * L.S, L.T)
+                dst[r].zero_()
+                if hi > lo:
+                    dst[r][: hi - lo].copy_(src[lo:hi])
+
+    def flat(self, shards: Sequence[torch.Tensor]) -> torch.Tensor:
+        return torch.cat(list(shards))[: self.layout.T]
+
+    def grad_table(self, grads: Sequence[Sequence[torch.Tensor]]) -> zr.PtrArray:
+        """Host array [world * n_params] of device pointers, built once per set of grads."""
+        return zr.PtrArray([t for row in grads for t in row])
+
+    # ---- the step -------------------------------------------------------------------
+    def pack(self, b: int, grad_table: zr.PtrArray, stream=None) -> None:
+        zr.zr_bucket_pack(self.layout, b, grad_table, self._p_buckets, dtype=self.zr_dtype, stream=stream)
+
+    def fused(self, b: int, hp, bucket_in: Optional[zr.PtrArray] = None, shard_grad_out=None,
+              write_param: bool = True, stream=None) -> None:
+        zr.zr_rs_adam_fused(self.layout, b, bucket_in or self._p_buckets, self.scale, self._p_master,
+                            self._p_m, self._p_v, hp, self.param if write_param else None,
+                            shard_grad_out, dtype=self.zr_dtype, stream=stream)
+
+    def step(self, grad_table: zr.PtrArray, hp, stream=None) -> None:
+        """Every bucket in order: pack each rank's grads, then the fused step."""
+        for b in range(self.layout.n_buckets):
+            self.pack(b, grad_table, stream)
+            self.fused(b, hp, stream=stream)
+
+    def main_grad_views(self, main_grad: Sequence[torch.Tensor]) -> List[zr.PtrArray]:
+        """Per-bucket pointer arrays into flat [P] fp32 per-rank grad buffers: the
+        Megatron-style contiguous buffer is already bucket-ordered, so its
+        buckets are read in place without packing."""
+        es = main_grad[0].element_size()
+        out = []
+        for b in range(self.layout.n_buckets):
+            start, _ = self.layout.bucket(b)
+            out.append(zr.PtrArray([t.data_ptr() + start * es for t in main_grad]))
+        return out
+
+    def step_in_place(self, bucket_views: Sequence[zr.PtrArray], hp, stream=None) -> None:
+        for b in range(self.layout.n_buckets):
+            self.fused(b, hp, bucket_in=bucket_views[b], stream=stream)

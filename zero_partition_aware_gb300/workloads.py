@@ -159,6 +159,18 @@ def draw_inputs(wl: Workload, device="cpu", seed: int = 0, n: Optional[int] = No
     return {"master": master, "grads": grads, "m": m, "v": v}
 
 
+def arena_offsets(numel: Sequence[int], align: int = 256) -> List[int]:
+    """Start of each tensor when the tensors are allocated one after another in
+    one arena, each start rounded up to `align` elements (as separately
+    allocated gradient tensors would sit in memory). align=1 packs them."""
+    out, pos = [], 0
+    for n in numel:
+        pos = -(-pos // align) * align
+        out.append(pos)
+        pos += int(n)
+    return out
+
+
 def random_numels(rng: np.random.Generator, n: int, lo: int = 1, hi: int = 4000,
                   log: bool = True) -> List[int]:
     """Seeded element counts for small parity layouts (log-uniform by default)."""
@@ -178,5 +190,5 @@ def from_bf16_bits(a: np.ndarray) -> torch.Tensor:
 
 
 __all__ = ["AdamW", "Workload", "WORKLOADS", "draw_inputs", "draw_grad", "draw_state",
-           "generator", "replace", "random_numels", "bf16_bits", "from_bf16_bits",
+           "generator", "replace", "random_numels", "arena_offsets", "bf16_bits", "from_bf16_bits",
            "gpt2_small_numel", "llama_numel", "irregular_numel"]

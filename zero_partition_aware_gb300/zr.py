@@ -1,0 +1,391 @@
+"""Thin ctypes binding of libzr (include/zr.h), same names as the C entry points.
+
+Argument marshalling only: tensors become device addresses, lists of tensors
+become host arrays of device pointers, the current torch stream becomes the
+launch stream. Every step runs in libzr's sm_103a kernels; there is no
+fallback. Importing this module raises ImportError if libzr.so has not been
+built (``python -c "import __graft_entry__ as g; g.build()"``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, Optional, Sequence, Union
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libzr.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libzr.so is not built ({_LIB_PATH} missing); run zero_partition_aware_gb300.build.build()")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+ZR_OK = 0
+ZR_ERR_INVALID_ARG = -1
+ZR_ERR_CUDA = -2
+ZR_ERR_OOM = -3
+ZR_ERR_ALIGN = -4
+ZR_ERR_TIMEOUT = -5
+ZR_ERR_STATE = -6
+ZR_ERR_UNSUPPORTED = -7
+ZR_BF16, ZR_FP32 = 0, 1
+ZR_MAX_WORLD = 1024
+ZR_DEFAULT_REDUCE_BUCKET_SIZE = 500_000_000
+ZR_DEFAULT_REDUCE_SCATTER = True
+ZR_DEFAULT_CONTIGUOUS_GRADIENTS = True
+ZR_DEFAULT_OVERLAP_COMM = False
+
+LIB_PATH = _LIB_PATH
+
+
+class ZrError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class zr_layout_info(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("P", ctypes.c_int64), ("S", ctypes.c_int64),
+                ("n_params", ctypes.c_int64), ("n_buckets", ctypes.c_int64),
+                ("n_slices", ctypes.c_int64), ("n_runs", ctypes.c_int64),
+                ("reduce_bucket_size", ctypes.c_int64), ("world", ctypes.c_int32)]
+
+
+class zr_slice(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_int64), ("bucket", ctypes.c_int64), ("dst", ctypes.c_int32),
+                ("param_offset", ctypes.c_int64), ("bucket_offset", ctypes.c_int64),
+                ("partition_offset", ctypes.c_int64), ("numel", ctypes.c_int64)]
+
+
+class zr_run(ctypes.Structure):
+    _fields_ = [("bucket", ctypes.c_int64), ("dst", ctypes.c_int32), ("bucket_offset", ctypes.c_int64),
+                ("partition_offset", ctypes.c_int64), ("numel", ctypes.c_int64)]
+
+
+class zr_adamw(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
+
+
+class zr_adamw_scalars(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in ("beta1", "one_minus_beta1", "beta2", "one_minus_beta2",
+                                                "step_size", "bc2_sqrt", "decay", "eps")]
+
+
+_vp = ctypes.c_void_p
+_i32, _i64, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+_P = ctypes.POINTER
+
+_SIGS = {
+    "zr_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "zr_last_error": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_size_t]),
+    "zr_version": (ctypes.c_int, []),
+    "zr_launch_count": (ctypes.c_int64, []),
+    "zr_layout_create": (ctypes.c_int, [_vp, _i64, _i32, _i64, _P(_vp)]),
+    "zr_layout_destroy": (ctypes.c_int, [_vp]),
+    "zr_layout_query": (ctypes.c_int, [_vp, _P(zr_layout_info)]),
+    "zr_layout_param_partitions": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _P(_i32)]),
+    "zr_layout_slices": (ctypes.c_int, [_vp, _vp, _i64, _P(_i64)]),
+    "zr_layout_runs": (ctypes.c_int, [_vp, _vp, _i64, _P(_i64)]),
+    "zr_layout_bucket": (ctypes.c_int, [_vp, _i64, _P(_i64), _P(_i64)]),
+    "zr_layout_param": (ctypes.c_int, [_vp, _i64, _P(_i64), _P(_i64)]),
+    "zr_bucket_pack": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
+    "zr_grad_accumulate": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
+    "zr_reduce_scatter_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
+    "zr_adam_shard_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _P(zr_adamw), _vp]),
+    "zr_gather_cast_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "zr_rs_adam_fused": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp, _vp,
+                                        _P(zr_adamw), _vp, _vp, _vp]),
+    "zr_allreduce_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
+    "zr_adamw_prepare": (ctypes.c_int, [_P(zr_adamw), _P(zr_adamw_scalars)]),
+    "zr_comm_bytes": (ctypes.c_int, [_vp, _i32, _i32, _P(ctypes.c_double)]),
+    "zr_layout_bytes": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_double)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+def last_error() -> str:
+    buf = ctypes.create_string_buffer(1024)
+    _lib.zr_last_error(buf, len(buf))
+    return buf.value.decode(errors="replace")
+
+
+def _check(rc: int, what: str):
+    if rc != ZR_OK:
+        raise ZrError(rc, f"{what}: {last_error() or _lib.zr_status_string(rc).decode()}")
+
+
+# ----------------------------------------------------------------------------
+# Marshalling helpers
+# ----------------------------------------------------------------------------
+
+def _addr(x) -> Optional[int]:
+    """Device address of a tensor, or an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_cuda:
+            raise ValueError("libzr takes CUDA tensors; got a CPU tensor")
+        if not x.is_contiguous():
+            raise ValueError("libzr takes contiguous tensors")
+        return x.data_ptr()
+    raise TypeError(f"cannot take a device address of {type(x)}")
+
+
+class PtrArray:
+    """A host array of device pointers, built once and reusable across calls."""
+
+    def __init__(self, items: Iterable):
+        vals = [_addr(t) or 0 for t in items]
+        self.array = np.asarray(vals, dtype=np.uint64)
+        self._keep = list(items) if not isinstance(items, np.ndarray) else None
+
+    @property
+    def ptr(self) -> int:
+        return self.array.ctypes.data
+
+    def __len__(self):
+        return int(self.array.shape[0])
+
+
+def _ptrs(x) -> Optional[PtrArray]:
+    if x is None:
+        return None
+    if isinstance(x, PtrArray):
+        return x
+    return PtrArray(x)
+
+
+def _dtype_of(x, dtype) -> int:
+    if dtype is not None:
+        return int(dtype)
+    import torch
+    seq = x
+    while isinstance(seq, (list, tuple)):
+        seq = next((s for s in seq if s is not None), None)
+    if isinstance(seq, PtrArray):
+        raise ValueError("dtype is required with a prebuilt PtrArray")
+    if seq is not None and hasattr(seq, "dtype"):
+        if seq.dtype == torch.bfloat16:
+            return ZR_BF16
+        if seq.dtype == torch.float32:
+            return ZR_FP32
+    raise ValueError("cannot infer dtype: pass dtype=ZR_BF16 or ZR_FP32")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _hp(hp) -> zr_adamw:
+    if isinstance(hp, zr_adamw):
+        return hp
+    return zr_adamw(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, int(hp.step))
+
+
+# ----------------------------------------------------------------------------
+# Layout
+# ----------------------------------------------------------------------------
+
+class Layout:
+    """Owns a zr_layout handle (host memory only)."""
+
+    def __init__(self, numel: Sequence[int], world: int,
+                 reduce_bucket_size: int = ZR_DEFAULT_REDUCE_BUCKET_SIZE):
+        arr = np.ascontiguousarray(np.asarray(numel, dtype=np.int64))
+        h = ctypes.c_void_p()
+        _check(_lib.zr_layout_create(arr.ctypes.data if arr.size else None, int(arr.size), int(world),
+                                     int(reduce_bucket_size), ctypes.byref(h)), "zr_layout_create")
+        self._h = h
+        info = zr_layout_info()
+        _check(_lib.zr_layout_query(h, ctypes.byref(info)), "zr_layout_query")
+        self.info = info
+        self.numel = arr
+        self._bucket_cache = {}
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.zr_layout_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    T = property(lambda s: int(s.info.T))
+    P = property(lambda s: int(s.info.P))
+    S = property(lambda s: int(s.info.S))
+    world = property(lambda s: int(s.info.world))
+    n_params = property(lambda s: int(s.info.n_params))
+    n_buckets = property(lambda s: int(s.info.n_buckets))
+    n_slices = property(lambda s: int(s.info.n_slices))
+    n_runs = property(lambda s: int(s.info.n_runs))
+    reduce_bucket_size = property(lambda s: int(s.info.reduce_bucket_size))
+
+    def bucket(self, b: int):
+        """(flat_start, numel) of bucket b."""
+        if b not in self._bucket_cache:
+            s, n = ctypes.c_int64(), ctypes.c_int64()
+            _check(_lib.zr_layout_bucket(self._h, int(b), ctypes.byref(s), ctypes.byref(n)), "zr_layout_bucket")
+            self._bucket_cache[b] = (s.value, n.value)
+        return self._bucket_cache[b]
+
+    def param(self, i: int):
+        """(flat_offset, bucket) of param i."""
+        o, b = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.zr_layout_param(self._h, int(i), ctypes.byref(o), ctypes.byref(b)), "zr_layout_param")
+        return o.value, b.value
+
+    def param_partitions(self, i: int):
+        """(param_to_partition_ids, grad_start_offset) of param i."""
+        n = ctypes.c_int32()
+        _check(_lib.zr_layout_param_partitions(self._h, int(i), None, None, 0, ctypes.byref(n)),
+               "zr_layout_param_partitions")
+        ids = np.zeros(max(n.value, 1), np.int32)
+        gso = np.zeros(max(n.value, 1), np.int64)
+        _check(_lib.zr_layout_param_partitions(self._h, int(i), ids.ctypes.data, gso.ctypes.data,
+                                               n.value, ctypes.byref(n)), "zr_layout_param_partitions")
+        return [int(x) for x in ids[: n.value]], [int(x) for x in gso[: n.value]]
+
+    def slices(self) -> np.ndarray:
+        """[n_slices, 7]: param, bucket, dst, param_offset, bucket_offset, partition_offset, numel."""
+        n = ctypes.c_int64()
+        _check(_lib.zr_layout_slices(self._h, None, 0, ctypes.byref(n)), "zr_layout_slices")
+        buf = (zr_slice * max(n.value, 1))()
+        _check(_lib.zr_layout_slices(self._h, buf, n.value, ctypes.byref(n)), "zr_layout_slices")
+        return np.array([[s.param, s.bucket, s.dst, s.param_offset, s.bucket_offset, s.partition_offset,
+                          s.numel] for s in buf[: n.value]], dtype=np.int64).reshape(-1, 7)
+
+    def runs(self) -> np.ndarray:
+        """[n_runs, 5]: bucket, dst, bucket_offset, partition_offset, numel."""
+        n = ctypes.c_int64()
+        _check(_lib.zr_layout_runs(self._h, None, 0, ctypes.byref(n)), "zr_layout_runs")
+        buf = (zr_run * max(n.value, 1))()
+        _check(_lib.zr_layout_runs(self._h, buf, n.value, ctypes.byref(n)), "zr_layout_runs")
+        return np.array([[r.bucket, r.dst, r.bucket_offset, r.partition_offset, r.numel]
+                         for r in buf[: n.value]], dtype=np.int64).reshape(-1, 5)
+
+    def offsets(self) -> np.ndarray:
+        return np.array([self.param(i)[0] for i in range(self.n_params)], dtype=np.int64)
+
+
+def zr_layout_create(numel: Sequence[int], world: int,
+                     reduce_bucket_size: int = ZR_DEFAULT_REDUCE_BUCKET_SIZE) -> Layout:
+    return Layout(numel, world, reduce_bucket_size)
+
+
+def zr_layout_destroy(layout: Layout) -> None:
+    layout.close()
+
+
+# ----------------------------------------------------------------------------
+# Device steps
+# ----------------------------------------------------------------------------
+
+def zr_bucket_pack(layout: Layout, bucket: int, grads, bucket_out, dtype=None, stream=None) -> None:
+    """grads: [world][n_params] tensors (or a flat PtrArray of world*n_params);
+    bucket_out: [world] tensors of numel_b elements."""
+    if isinstance(grads, PtrArray):
+        g = grads
+    else:
+        g = PtrArray([t for row in grads for t in row])
+    d = _dtype_of(bucket_out, dtype)
+    o = _ptrs(bucket_out)
+    _check(_lib.zr_bucket_pack(layout.handle, int(bucket), g.ptr, d, o.ptr, _stream(stream)), "zr_bucket_pack")
+
+
+def zr_grad_accumulate(main_grad, g, n: Optional[int] = None, dtype=None, stream=None) -> None:
+    if n is None:
+        n = int(main_grad.numel())
+        if int(g.numel()) != n:
+            raise ValueError("main_grad and g sizes differ")
+    d = _dtype_of([g], dtype)
+    _check(_lib.zr_grad_accumulate(_addr(main_grad), _addr(g), d, int(n), _stream(stream)), "zr_grad_accumulate")
+
+
+def zr_reduce_scatter_avg(layout: Layout, bucket: int, bucket_in, scale: float, shard_grad,
+                          dtype=None, stream=None) -> None:
+    d = _dtype_of(bucket_in, dtype)
+    x, g = _ptrs(bucket_in), _ptrs(shard_grad)
+    _check(_lib.zr_reduce_scatter_avg(layout.handle, int(bucket), x.ptr, d, float(scale), g.ptr,
+                                      _stream(stream)), "zr_reduce_scatter_avg")
+
+
+def zr_adam_shard_step(layout: Layout, rank: int, master, m, v, grad, hp, stream=None) -> None:
+    h = _hp(hp)
+    _check(_lib.zr_adam_shard_step(layout.handle, int(rank), _ptrs(master).ptr, _ptrs(m).ptr, _ptrs(v).ptr,
+                                   _ptrs(grad).ptr, ctypes.byref(h), _stream(stream)), "zr_adam_shard_step")
+
+
+def zr_gather_cast_bf16(layout: Layout, master, param_bf16, stream=None) -> None:
+    _check(_lib.zr_gather_cast_bf16(layout.handle, _ptrs(master).ptr, _addr(param_bf16), _stream(stream)),
+           "zr_gather_cast_bf16")
+
+
+def zr_rs_adam_fused(layout: Layout, bucket: int, bucket_in, scale: float, master, m, v, hp,
+                     param_bf16=None, shard_grad_out=None, dtype=None, stream=None) -> None:
+    d = _dtype_of(bucket_in, dtype)
+    h = _hp(hp)
+    go = _ptrs(shard_grad_out)
+    _check(_lib.zr_rs_adam_fused(layout.handle, int(bucket), _ptrs(bucket_in).ptr, d, float(scale),
+                                 _ptrs(master).ptr, _ptrs(m).ptr, _ptrs(v).ptr, ctypes.byref(h),
+                                 _addr(param_bf16), go.ptr if go is not None else None, _stream(stream)),
+           "zr_rs_adam_fused")
+
+
+def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, dtype=None, stream=None) -> None:
+    d = _dtype_of(bucket_in, dtype)
+    _check(_lib.zr_allreduce_avg(layout.handle, int(bucket), _ptrs(bucket_in).ptr, d, float(scale),
+                                 _ptrs(out).ptr, _stream(stream)), "zr_allreduce_avg")
+
+
+# ----------------------------------------------------------------------------
+# Accounting
+# ----------------------------------------------------------------------------
+
+def zr_adamw_prepare(hp) -> dict:
+    h = _hp(hp)
+    out = zr_adamw_scalars()
+    _check(_lib.zr_adamw_prepare(ctypes.byref(h), ctypes.byref(out)), "zr_adamw_prepare")
+    return {n: getattr(out, n) for n, _ in zr_adamw_scalars._fields_}
+
+
+def zr_comm_bytes(layout: Layout, scheme: int, elem_bytes: int) -> float:
+    out = ctypes.c_double()
+    _check(_lib.zr_comm_bytes(layout.handle, int(scheme), int(elem_bytes), ctypes.byref(out)), "zr_comm_bytes")
+    return out.value
+
+
+def zr_layout_bytes(layout: Layout, stage: int) -> float:
+    out = ctypes.c_double()
+    _check(_lib.zr_layout_bytes(layout.handle, int(stage), ctypes.byref(out)), "zr_layout_bytes")
+    return out.value
+
+
+def zr_status_string(status: int) -> str:
+    return _lib.zr_status_string(int(status)).decode()
+
+
+def zr_version() -> int:
+    return int(_lib.zr_version())
+
+
+def zr_launch_count() -> int:
+    return int(_lib.zr_launch_count())
