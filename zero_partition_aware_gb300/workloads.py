@@ -111,6 +111,14 @@ WORKLOADS = {
 }
 
 
+# A small slice of the irregular workload for profiler captures: its first 400
+# params (world 16, 2^24 buckets); each bucket's working set still exceeds L2.
+WORKLOADS["irregular_prof"] = Workload(
+    "irregular_prof", WORKLOADS["irregular_10k"].numel[:400], 16, 1 << 24,
+    ("int", -8, 8), 0.02, ("zero",), AdamW(step=1),
+    description="first 400 params of irregular_10k, world=16, bucket 2^24 (profiling size)")
+
+
 def replace(wl: Workload, **kw) -> Workload:
     return dataclasses.replace(wl, **kw)
 
