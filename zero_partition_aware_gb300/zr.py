@@ -330,12 +330,15 @@ def zr_reduce_scatter_avg(layout: Layout, bucket: int, bucket_in, scale: float, 
 
 def zr_adam_shard_step(layout: Layout, rank: int, master, m, v, grad, hp, stream=None) -> None:
     h = _hp(hp)
-    _check(_lib.zr_adam_shard_step(layout.handle, int(rank), _ptrs(master).ptr, _ptrs(m).ptr, _ptrs(v).ptr,
-                                   _ptrs(grad).ptr, ctypes.byref(h), _stream(stream)), "zr_adam_shard_step")
+    # the host pointer tables must outlive the call: keep them in locals
+    pm, pmm, pv, pg = _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(grad)
+    _check(_lib.zr_adam_shard_step(layout.handle, int(rank), pm.ptr, pmm.ptr, pv.ptr, pg.ptr,
+                                   ctypes.byref(h), _stream(stream)), "zr_adam_shard_step")
 
 
 def zr_gather_cast_bf16(layout: Layout, master, param_bf16, stream=None) -> None:
-    _check(_lib.zr_gather_cast_bf16(layout.handle, _ptrs(master).ptr, _addr(param_bf16), _stream(stream)),
+    pm = _ptrs(master)
+    _check(_lib.zr_gather_cast_bf16(layout.handle, pm.ptr, _addr(param_bf16), _stream(stream)),
            "zr_gather_cast_bf16")
 
 
@@ -343,17 +346,17 @@ def zr_rs_adam_fused(layout: Layout, bucket: int, bucket_in, scale: float, maste
                      param_bf16=None, shard_grad_out=None, dtype=None, stream=None) -> None:
     d = _dtype_of(bucket_in, dtype)
     h = _hp(hp)
-    go = _ptrs(shard_grad_out)
-    _check(_lib.zr_rs_adam_fused(layout.handle, int(bucket), _ptrs(bucket_in).ptr, d, float(scale),
-                                 _ptrs(master).ptr, _ptrs(m).ptr, _ptrs(v).ptr, ctypes.byref(h),
-                                 _addr(param_bf16), go.ptr if go is not None else None, _stream(stream)),
-           "zr_rs_adam_fused")
+    px, pm, pmm, pv, go = _ptrs(bucket_in), _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(shard_grad_out)
+    _check(_lib.zr_rs_adam_fused(layout.handle, int(bucket), px.ptr, d, float(scale), pm.ptr, pmm.ptr, pv.ptr,
+                                 ctypes.byref(h), _addr(param_bf16), go.ptr if go is not None else None,
+                                 _stream(stream)), "zr_rs_adam_fused")
 
 
 def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, dtype=None, stream=None) -> None:
     d = _dtype_of(bucket_in, dtype)
-    _check(_lib.zr_allreduce_avg(layout.handle, int(bucket), _ptrs(bucket_in).ptr, d, float(scale),
-                                 _ptrs(out).ptr, _stream(stream)), "zr_allreduce_avg")
+    px, po = _ptrs(bucket_in), _ptrs(out)
+    _check(_lib.zr_allreduce_avg(layout.handle, int(bucket), px.ptr, d, float(scale), po.ptr, _stream(stream)),
+           "zr_allreduce_avg")
 
 
 # ----------------------------------------------------------------------------
