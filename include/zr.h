@@ -171,6 +171,23 @@ int zr_bucket_pack(const zr_layout *layout, int64_t bucket, const void *const *g
                    zr_dtype dtype, void *const *bucket_out, zr_stream stream);
 
 /*
+ * A pack plan: the segment descriptors of every bucket of `layout` for one set
+ * of gradient tensors and bucket buffers (same arguments as zr_bucket_pack),
+ * uploaded once to device memory so that each bucket is packed by a single
+ * launch. Training loops keep their gradient and bucket tensors across steps,
+ * so the plan is built once and reused; rebuild it if any pointer changes.
+ * The plan allocates device memory on the current device (about 48 bytes per
+ * (replica, param) pair) and copies to it synchronously; it holds the pointers
+ * it was given, not the tensors. Same packing semantics as zr_bucket_pack.
+ */
+typedef struct zr_pack_plan zr_pack_plan;
+int zr_pack_plan_create(const zr_layout *layout, const void *const *grads, zr_dtype dtype,
+                        void *const *bucket_out, zr_pack_plan **out);
+int zr_pack_plan_destroy(zr_pack_plan *plan);
+/* Packs bucket b of the plan: one kernel launch on `stream`. */
+int zr_bucket_pack_planned(const zr_pack_plan *plan, int64_t bucket, zr_stream stream);
+
+/*
  * fp32 main-grad accumulation ([MG] §"四步接力" step 2: main_grad.add_(grad)
  * into the fp32 contiguous buffer): main_grad[e] += float(g[e]), e < n.
  * main_grad: device fp32 [n], in/out. g: device [n] of g_dtype.

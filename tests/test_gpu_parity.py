@@ -167,6 +167,23 @@ def test_pack(zr, world, seed, n, hi, B, dtype):
         for k in range(world):
             outs[k].check_guards()
             assert np.array_equal(outs[k].bits(), want[k].view(outs[k].bits().dtype)), (b, k)
+    # the planned path: one launch per bucket from device-resident descriptors
+    mx = max(lay.bucket(b)[1] for b in range(lay.n_buckets))
+    outs = [Guarded(mx, tdt, ph) for ph in _rand_phases(rng, world, es)]
+    plan = zr.PackPlan(zl, table, [o.view for o in outs])
+    for b in range(lay.n_buckets):
+        _, nb = lay.bucket(b)
+        for o in outs:
+            o.view.view(torch.int16 if es == 2 else torch.int32).fill_(CANARY16 if es == 2 else CANARY32)
+        zr.zr_bucket_pack_planned(plan, b)
+        torch.cuda.synchronize()
+        want = oracle.bucket_pack(lay, b, grads_np)
+        for k in range(world):
+            outs[k].check_guards()
+            got = outs[k].bits()
+            assert np.array_equal(got[:nb], want[k].view(got.dtype)), (b, k)
+            assert np.all(got[nb:] == outs[k].canary), "planned pack wrote past the bucket"
+    plan.close()
     for g in keep:
         g.check_guards()
 
@@ -388,6 +405,50 @@ def test_empty_and_degenerate_calls(zr):
     assert g.item() == 1.5
 
 
+@pytest.mark.parametrize("world,dtype,phases", [(16, "bf16", "same"), (16, "bf16", "mixed"), (8, "fp32", "same"),
+                                                 (4, "bf16", "mixed"), (3, "bf16", "same")])
+def test_fused_medium_many_pipeline_tiles(zr, world, dtype, phases):
+    """A few million elements: most tiles go through the shared-memory pipeline; every element compared."""
+    rng = np.random.default_rng(world * 7 + len(phases))
+    numel = [int(x) for x in rng.integers(50_000, 400_000, 12)] + [1, 7, 1000]
+    B = 1_000_000
+    lay = oracle.layout(numel, world, B)
+    zl = zr.Layout(numel, world, B)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    es = 2 if dtype == "bf16" else 4
+    scale = float(np.float32(1.0 / world))
+    hp = W.AdamW(step=5)
+
+    def mk(arrs):
+        out = []
+        for r in range(world):
+            g = Guarded(lay.S, torch.float32, 0 if phases == "same" else int(rng.integers(0, 4)))
+            g.set(arrs[r])
+            out.append(g)
+        return out
+
+    flat = lambda std, absval=False: np.concatenate([_f32_np(rng, lay.T, std), np.zeros(lay.P - lay.T, np.float32)])
+    p_np = np.split(flat(0.02), world)
+    m_np = np.split(np.abs(flat(1e-4)), world)
+    v_np = np.split(np.abs(flat(1e-4)), world)
+    P_, M_, V_ = mk(p_np), mk(m_np), mk(v_np)
+    param = Guarded(lay.P, torch.bfloat16, int(rng.integers(0, 8)))
+    want = [[a.copy() for a in p_np], [a.copy() for a in m_np], [a.copy() for a in v_np]]
+    want_param = np.full(lay.P, CANARY16, np.uint16)
+    for b in range(lay.n_buckets):
+        vals, dev = _buckets_on_device(rng, lay, b, world, tdt, es)
+        zr.zr_rs_adam_fused(zl, b, [d.view for d in dev], scale, [x.view for x in P_], [x.view for x in M_],
+                            [x.view for x in V_], hp, param.view)
+        oracle.rs_adam_fused(lay, b, vals, scale, want[0], want[1], want[2], hp, want_param)
+        torch.cuda.synchronize()
+    for r in range(world):
+        for got, w, nm in ((P_, want[0], "p"), (M_, want[1], "m"), (V_, want[2], "v")):
+            got[r].check_guards()
+            _assert_same(got[r].bits(), w[r], f"{nm} rank {r}")
+    param.check_guards()
+    _assert_same(param.bits(), want_param, "param", dtype="bf16")
+
+
 def test_determinism(zr):
     rng, numel, lay = _case(16, 5, 40, 3000, 30000)
     zl = zr.Layout(numel, 16, 30000)
@@ -518,7 +579,7 @@ def test_full_size_workload_sampled(zr, name):
             inp["grads"][k][0] = None
             rows.append((arena, views))
         table = grp.grad_table([v for _, v in rows])
-        grp.step(table, wl.adam)
+        grp.step(table, wl.adam, plan=grp.pack_plan(table))
     torch.cuda.synchronize()
     # oracle, position by position
     avg = oracle.allreduce_avg(wl.world, x, grp.scale)[0]
@@ -533,3 +594,4 @@ def test_full_size_workload_sampled(zr, name):
     if name == "irregular_10k":
         # integer grads: the averaged gradient is exact, so the update is pinned by the closed form
         assert np.all(np.abs(avg * 16 - np.rint(avg * 16)) == 0)
+

@@ -71,16 +71,26 @@ class DPGroup:
     def pack(self, b: int, grad_table: zr.PtrArray, stream=None) -> None:
         zr.zr_bucket_pack(self.layout, b, grad_table, self._p_buckets, dtype=self.zr_dtype, stream=stream)
 
+    def pack_plan(self, grad_table: zr.PtrArray) -> zr.PackPlan:
+        """Device-resident packing descriptors for these gradient tensors (build once)."""
+        return zr.PackPlan(self.layout, grad_table, self._p_buckets, dtype=self.zr_dtype)
+
+    def pack_planned(self, b: int, plan: zr.PackPlan, stream=None) -> None:
+        zr.zr_bucket_pack_planned(plan, b, stream=stream)
+
     def fused(self, b: int, hp, bucket_in: Optional[zr.PtrArray] = None, shard_grad_out=None,
               write_param: bool = True, stream=None) -> None:
         zr.zr_rs_adam_fused(self.layout, b, bucket_in or self._p_buckets, self.scale, self._p_master,
                             self._p_m, self._p_v, hp, self.param if write_param else None,
                             shard_grad_out, dtype=self.zr_dtype, stream=stream)
 
-    def step(self, grad_table: zr.PtrArray, hp, stream=None) -> None:
+    def step(self, grad_table: zr.PtrArray, hp, stream=None, plan: Optional[zr.PackPlan] = None) -> None:
         """Every bucket in order: pack each rank's grads, then the fused step."""
         for b in range(self.layout.n_buckets):
-            self.pack(b, grad_table, stream)
+            if plan is not None:
+                self.pack_planned(b, plan, stream)
+            else:
+                self.pack(b, grad_table, stream)
             self.fused(b, hp, stream=stream)
 
     def main_grad_views(self, main_grad: Sequence[torch.Tensor]) -> List[zr.PtrArray]:

@@ -89,6 +89,9 @@ _SIGS = {
     "zr_layout_bucket": (ctypes.c_int, [_vp, _i64, _P(_i64), _P(_i64)]),
     "zr_layout_param": (ctypes.c_int, [_vp, _i64, _P(_i64), _P(_i64)]),
     "zr_bucket_pack": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
+    "zr_pack_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _P(_vp)]),
+    "zr_pack_plan_destroy": (ctypes.c_int, [_vp]),
+    "zr_bucket_pack_planned": (ctypes.c_int, [_vp, _i64, _vp]),
     "zr_grad_accumulate": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_reduce_scatter_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
     "zr_adam_shard_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _P(zr_adamw), _vp]),
@@ -309,6 +312,47 @@ def zr_bucket_pack(layout: Layout, bucket: int, grads, bucket_out, dtype=None, s
     d = _dtype_of(bucket_out, dtype)
     o = _ptrs(bucket_out)
     _check(_lib.zr_bucket_pack(layout.handle, int(bucket), g.ptr, d, o.ptr, _stream(stream)), "zr_bucket_pack")
+
+
+class PackPlan:
+    """Owns a zr_pack_plan: device-resident packing descriptors for fixed
+    gradient tensors and bucket buffers (one launch per bucket)."""
+
+    def __init__(self, layout: Layout, grads, bucket_out, dtype=None):
+        g = grads if isinstance(grads, PtrArray) else PtrArray([t for row in grads for t in row])
+        o = _ptrs(bucket_out)
+        d = _dtype_of(bucket_out, dtype)
+        h = ctypes.c_void_p()
+        _check(_lib.zr_pack_plan_create(layout.handle, g.ptr, d, o.ptr, ctypes.byref(h)), "zr_pack_plan_create")
+        self._h = h
+        self._keep = (layout, g, o)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.zr_pack_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def zr_pack_plan_create(layout: Layout, grads, bucket_out, dtype=None) -> PackPlan:
+    return PackPlan(layout, grads, bucket_out, dtype)
+
+
+def zr_pack_plan_destroy(plan: PackPlan) -> None:
+    plan.close()
+
+
+def zr_bucket_pack_planned(plan: PackPlan, bucket: int, stream=None) -> None:
+    _check(_lib.zr_bucket_pack_planned(plan.handle, int(bucket), _stream(stream)), "zr_bucket_pack_planned")
 
 
 def zr_grad_accumulate(main_grad, g, n: Optional[int] = None, dtype=None, stream=None) -> None:
