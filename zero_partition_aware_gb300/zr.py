@@ -92,6 +92,7 @@ _SIGS = {
     "zr_pack_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _P(_vp)]),
     "zr_pack_plan_destroy": (ctypes.c_int, [_vp]),
     "zr_bucket_pack_planned": (ctypes.c_int, [_vp, _i64, _vp]),
+    "zr_bucket_pack_noalloc": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
     "zr_grad_accumulate": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_reduce_scatter_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
     "zr_adam_shard_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _P(zr_adamw), _vp]),
@@ -312,6 +313,15 @@ def zr_bucket_pack(layout: Layout, bucket: int, grads, bucket_out, dtype=None, s
     d = _dtype_of(bucket_out, dtype)
     o = _ptrs(bucket_out)
     _check(_lib.zr_bucket_pack(layout.handle, int(bucket), g.ptr, d, o.ptr, _stream(stream)), "zr_bucket_pack")
+
+
+def zr_bucket_pack_noalloc(layout: Layout, bucket: int, grads, bucket_out, dtype=None, stream=None) -> None:
+    """zr_bucket_pack that allocates no device memory (see include/zr.h)."""
+    g = grads if isinstance(grads, PtrArray) else PtrArray([t for row in grads for t in row])
+    d = _dtype_of(bucket_out, dtype)
+    o = _ptrs(bucket_out)
+    _check(_lib.zr_bucket_pack_noalloc(layout.handle, int(bucket), g.ptr, d, o.ptr, _stream(stream)),
+           "zr_bucket_pack_noalloc")
 
 
 class PackPlan:
