@@ -275,6 +275,26 @@ int zr_rs_adam_fused(const zr_layout *layout, int64_t bucket, const void *const 
                      float *const *shard_grad_out, zr_stream stream);
 
 /*
+ * Steps 1 to 4 in one pass, without a bucket buffer. A direct plan records,
+ * once, where every replica's gradient of every param of every bucket lives
+ * (grads as for zr_bucket_pack; the tensors must stay allocated while the plan
+ * is used) and how the bucket positions map to params, in device memory the
+ * plan owns (8 bytes per replica and param, plus about 12 bytes per param and
+ * 4 per 256 bucket positions). zr_step_direct then does for bucket b what
+ * zr_bucket_pack followed by zr_rs_adam_fused does, with identical results:
+ * each replica's slice of each param is read where it lies, by its
+ * grad_start_offset, instead of being packed first ([DS] §三.2 slicing by
+ * param_to_partition_ids / grad_start_offset; [DS] §四). world <= 32.
+ */
+typedef struct zr_direct_plan zr_direct_plan;
+int zr_direct_plan_create(const zr_layout *layout, const void *const *grads, zr_dtype dtype,
+                          zr_direct_plan **out);
+int zr_direct_plan_destroy(zr_direct_plan *plan);
+int zr_step_direct(const zr_direct_plan *plan, int64_t bucket, float scale, float *const *master,
+                   float *const *m, float *const *v, const zr_adamw *hp, void *param_bf16,
+                   float *const *shard_grad_out, zr_stream stream);
+
+/*
  * All-reduce with average over one bucket, the path used when
  * reduce_scatter is off ([DS] §三.2 gradient_reduction_w_predivide; [MG]
  * §"四步接力" step 4; [IQ] §"三种原语"): out[k][e] = the same averaged value

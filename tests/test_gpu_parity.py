@@ -449,6 +449,75 @@ def test_fused_medium_many_pipeline_tiles(zr, world, dtype, phases):
     _assert_same(param.bits(), want_param, "param", dtype="bf16")
 
 
+@pytest.mark.parametrize("world,seed,n,hi,B", [c for c in CASES if c[0] <= 32] + [(16, 9, 30, 300_000, 2_000_000)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("phases", ["same", "mixed"])
+def test_step_direct(zr, world, seed, n, hi, B, dtype, phases):
+    """Steps 1-4 from per-parameter tensors without a bucket buffer == oracle pack + fused step."""
+    rng, numel, lay = _case(world, seed, n, hi, B)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    es = 2 if dtype == "bf16" else 4
+    zl = zr.Layout(numel, world, B)
+    scale = float(np.float32(1.0 / world))
+    hp = W.AdamW(step=int(rng.integers(1, 20)))
+    grads_np = [[(_bf16_np(rng, m) if dtype == "bf16" else _f32_np(rng, m, 1e-2)) for m in numel]
+                for _ in range(world)]
+    grads_dev, keep = [], []
+    for k in range(world):
+        row = []
+        if k % 2 == 0:
+            flat = np.concatenate(grads_np[k])
+            g = Guarded(len(flat), tdt, int(rng.integers(0, 16 // es)))
+            g.set(flat)
+            keep.append(g)
+            pos = 0
+            for m in numel:
+                row.append(g.view[pos:pos + m])
+                pos += m
+        else:
+            for i, m in enumerate(numel):
+                g = Guarded(m, tdt, int(rng.integers(0, 16 // es)))
+                g.set(grads_np[k][i])
+                keep.append(g)
+                row.append(g.view)
+        grads_dev.append(row)
+    plan = zr.DirectPlan(zl, grads_dev)
+
+    def mk(arrs):
+        out = []
+        for r in range(world):
+            gg = Guarded(lay.S, torch.float32, 0 if phases == "same" else int(rng.integers(0, 4)))
+            gg.set(arrs[r])
+            out.append(gg)
+        return out
+
+    flat = lambda std: np.concatenate([_f32_np(rng, lay.T, std), np.zeros(lay.P - lay.T, np.float32)])
+    p_np = np.split(flat(0.02), world)
+    m_np = np.split(np.abs(flat(1e-4)), world)
+    v_np = np.split(np.abs(flat(1e-4)), world)
+    P_, M_, V_ = mk(p_np), mk(m_np), mk(v_np)
+    G_ = mk([np.full(lay.S, np.float32(np.nan), np.float32) for _ in range(world)])
+    param = Guarded(lay.P, torch.bfloat16, int(rng.integers(0, 8)))
+    want = [[a.copy() for a in p_np], [a.copy() for a in m_np], [a.copy() for a in v_np],
+            [np.full(lay.S, np.float32(np.nan), np.float32) for _ in range(world)]]
+    want_param = np.full(lay.P, CANARY16, np.uint16)
+    for b in range(lay.n_buckets):
+        zr.zr_step_direct(plan, b, scale, [x.view for x in P_], [x.view for x in M_], [x.view for x in V_], hp,
+                          param.view, [x.view for x in G_])
+        bucket = oracle.bucket_pack(lay, b, grads_np)
+        oracle.rs_adam_fused(lay, b, bucket, scale, want[0], want[1], want[2], hp, want_param, want[3])
+    torch.cuda.synchronize()
+    for r in range(world):
+        for got, w, nm in ((P_, want[0], "p"), (M_, want[1], "m"), (V_, want[2], "v"), (G_, want[3], "g")):
+            got[r].check_guards()
+            _assert_same(got[r].bits(), w[r], f"direct {nm} rank {r}")
+    param.check_guards()
+    _assert_same(param.bits(), want_param, "direct param", dtype="bf16")
+    for g in keep:
+        g.check_guards()
+    plan.close()
+
+
 def test_determinism(zr):
     rng, numel, lay = _case(16, 5, 40, 3000, 30000)
     zl = zr.Layout(numel, 16, 30000)
@@ -522,8 +591,9 @@ def _gather_flat(tensors_by_rank, lay, f):
     return out
 
 
-@pytest.mark.parametrize("name", ["gpt2_124m", "llama_1p1b", "irregular_10k", "llama3_3b"])
-def test_full_size_workload_sampled(zr, name):
+@pytest.mark.parametrize("name,direct", [("gpt2_124m", False), ("llama_1p1b", False), ("irregular_10k", False),
+                                         ("llama3_3b", False), ("irregular_10k", True), ("gpt2_124m", True)])
+def test_full_size_workload_sampled(zr, name, direct):
     """Full-size workload, launched exactly as bench.py launches it, checked at sampled positions."""
     from zero_partition_aware_gb300.engine import DPGroup
     wl = W.WORKLOADS[name]
@@ -534,7 +604,7 @@ def test_full_size_workload_sampled(zr, name):
     inp = W.draw_inputs(wl, "cuda", seed=0)
     fp32_path = wl.micro_steps > 1
     grp = DPGroup(list(wl.numel), wl.world, wl.bucket, grad_dtype=torch.float32 if fp32_path else torch.bfloat16,
-                  allocate_buckets=not fp32_path)
+                  allocate_buckets=not (fp32_path or direct))
     grp.load_flat(inp["master"], inp["m"], inp["v"])
     del inp["master"], inp["m"], inp["v"]
     p0 = _gather_flat(grp.master, lay, f)
@@ -579,7 +649,10 @@ def test_full_size_workload_sampled(zr, name):
             inp["grads"][k][0] = None
             rows.append((arena, views))
         table = grp.grad_table([v for _, v in rows])
-        grp.step(table, wl.adam, plan=grp.pack_plan(table))
+        if direct:
+            grp.step_direct(grp.direct_plan(table), wl.adam)
+        else:
+            grp.step(table, wl.adam, plan=grp.pack_plan(table))
     torch.cuda.synchronize()
     # oracle, position by position
     avg = oracle.allreduce_avg(wl.world, x, grp.scale)[0]

@@ -93,6 +93,20 @@ class DPGroup:
                 self.pack(b, grad_table, stream)
             self.fused(b, hp, stream=stream)
 
+    def direct_plan(self, grad_table: zr.PtrArray) -> zr.DirectPlan:
+        """Device-resident map of these gradient tensors for the direct step (build once)."""
+        return zr.DirectPlan(self.layout, grad_table, dtype=self.zr_dtype)
+
+    def direct(self, b: int, plan: zr.DirectPlan, hp, shard_grad_out=None, write_param: bool = True,
+               stream=None) -> None:
+        zr.zr_step_direct(plan, b, self.scale, self._p_master, self._p_m, self._p_v, hp,
+                          self.param if write_param else None, shard_grad_out, stream=stream)
+
+    def step_direct(self, plan: zr.DirectPlan, hp, stream=None) -> None:
+        """Every bucket in order, steps 1-4 in one pass each, no bucket buffer."""
+        for b in range(self.layout.n_buckets):
+            self.direct(b, plan, hp, stream=stream)
+
     def main_grad_views(self, main_grad: Sequence[torch.Tensor]) -> List[zr.PtrArray]:
         """Per-bucket pointer arrays into flat [P] fp32 per-rank grad buffers: the
         Megatron-style contiguous buffer is already bucket-ordered, so its

@@ -100,6 +100,9 @@ _SIGS = {
     "zr_rs_adam_fused": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp, _vp,
                                         _P(zr_adamw), _vp, _vp, _vp]),
     "zr_allreduce_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
+    "zr_direct_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _P(_vp)]),
+    "zr_direct_plan_destroy": (ctypes.c_int, [_vp]),
+    "zr_step_direct": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
     "zr_adamw_prepare": (ctypes.c_int, [_P(zr_adamw), _P(zr_adamw_scalars)]),
     "zr_comm_bytes": (ctypes.c_int, [_vp, _i32, _i32, _P(ctypes.c_double)]),
     "zr_layout_bytes": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_double)]),
@@ -404,6 +407,54 @@ def zr_rs_adam_fused(layout: Layout, bucket: int, bucket_in, scale: float, maste
     _check(_lib.zr_rs_adam_fused(layout.handle, int(bucket), px.ptr, d, float(scale), pm.ptr, pmm.ptr, pv.ptr,
                                  ctypes.byref(h), _addr(param_bf16), go.ptr if go is not None else None,
                                  _stream(stream)), "zr_rs_adam_fused")
+
+
+class DirectPlan:
+    """Owns a zr_direct_plan: where every replica's per-parameter gradients live,
+    in device memory, for zr_step_direct (steps 1-4 without a bucket buffer)."""
+
+    def __init__(self, layout: Layout, grads, dtype=None):
+        g = grads if isinstance(grads, PtrArray) else PtrArray([t for row in grads for t in row])
+        if dtype is None:
+            if isinstance(grads, PtrArray):
+                raise ValueError("dtype is required with a prebuilt PtrArray")
+            dtype = _dtype_of([t for row in grads for t in row], None)
+        h = ctypes.c_void_p()
+        _check(_lib.zr_direct_plan_create(layout.handle, g.ptr, int(dtype), ctypes.byref(h)), "zr_direct_plan_create")
+        self._h = h
+        self._keep = (layout, g)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.zr_direct_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def zr_direct_plan_create(layout: Layout, grads, dtype=None) -> DirectPlan:
+    return DirectPlan(layout, grads, dtype)
+
+
+def zr_direct_plan_destroy(plan: DirectPlan) -> None:
+    plan.close()
+
+
+def zr_step_direct(plan: DirectPlan, bucket: int, scale: float, master, m, v, hp, param_bf16=None,
+                   shard_grad_out=None, stream=None) -> None:
+    h = _hp(hp)
+    pm, pmm, pv, go = _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(shard_grad_out)
+    _check(_lib.zr_step_direct(plan.handle, int(bucket), float(scale), pm.ptr, pmm.ptr, pv.ptr, ctypes.byref(h),
+                               _addr(param_bf16), go.ptr if go is not None else None, _stream(stream)),
+           "zr_step_direct")
 
 
 def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, dtype=None, stream=None) -> None:
