@@ -304,6 +304,33 @@ int zr_step_direct(const zr_direct_plan *plan, int64_t bucket, float scale, floa
 int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
                      zr_dtype dtype, float scale, float *const *out, zr_stream stream);
 
+/* ---- arithmetic self-check (device) -------------------------------------- */
+
+/*
+ * Compares, on the current device, the arithmetic the AdamW kernels use
+ * with CUDA's IEEE-754 operations (sqrt.rn, rcp.rn, div.rn). The kernels
+ * take the square root and the two divisions of the AdamW update ([DS]
+ * §四; torch.optim.AdamW's order of operations) through the hardware's
+ * approximate reciprocal (square root) and exact fma residuals (Markstein's
+ * method); this checks that they round as the IEEE operations do. The pages
+ * have no counterpart: it is a check of this library's arithmetic.
+ *   which 0: sqrt of every float bit pattern in [begin, begin + count);
+ *         1: reciprocal of every bit pattern in [begin, begin + count) whose
+ *            magnitude lies in [2^-60, 2^61) (the range the kernels use it in);
+ *         2: count random quotients a / b drawn by splitmix64 from index
+ *            begin + i (most inside that range, 1 in 16 any bit pattern),
+ *            each with a second, near-exact pair a = RN(b q);
+ *         3: count random AdamW elements (p, m, v, g over several decades)
+ *            under `hp`, compared with the element computed by the IEEE
+ *            operations (p, m and v bit for bit).
+ * For which 0 and 1, begin + count <= 2^32. hp is read for which 3 only.
+ * Writes the mismatch count to *mismatches and up to min(n_bad, 8) of the
+ * offending indices to bad (may be NULL). Allocates a few bytes of device
+ * memory and blocks until the check is done (device-wide synchronize).
+ */
+int zr_arith_check(int32_t which, uint64_t begin, uint64_t count, const zr_adamw *hp,
+                   uint64_t *mismatches, uint64_t *bad, int32_t n_bad);
+
 /* ---- accounting (host only) -------------------------------------------- */
 
 /* The AdamW scalars the kernels use for `hp` (see zr_adamw_scalars). */

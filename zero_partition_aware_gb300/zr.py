@@ -104,6 +104,8 @@ _SIGS = {
     "zr_direct_plan_destroy": (ctypes.c_int, [_vp]),
     "zr_step_direct": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
     "zr_adamw_prepare": (ctypes.c_int, [_P(zr_adamw), _P(zr_adamw_scalars)]),
+    "zr_arith_check": (ctypes.c_int, [_i32, ctypes.c_uint64, ctypes.c_uint64, _P(zr_adamw),
+                                      _P(ctypes.c_uint64), _P(ctypes.c_uint64), _i32]),
     "zr_comm_bytes": (ctypes.c_int, [_vp, _i32, _i32, _P(ctypes.c_double)]),
     "zr_layout_bytes": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_double)]),
 }
@@ -467,6 +469,16 @@ def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, 
 # ----------------------------------------------------------------------------
 # Accounting
 # ----------------------------------------------------------------------------
+
+def zr_arith_check(which: int, begin: int, count: int, hp=None):
+    """(mismatches, first offending indices) of the device arithmetic check."""
+    h = _hp(hp) if hp is not None else zr_adamw(1e-3, 0.9, 0.999, 1e-8, 0.0, 1)
+    n = ctypes.c_uint64()
+    bad = (ctypes.c_uint64 * 8)()
+    _check(_lib.zr_arith_check(int(which), int(begin), int(count), ctypes.byref(h), ctypes.byref(n), bad, 8),
+           "zr_arith_check")
+    return n.value, list(bad[: min(n.value, 8)])
+
 
 def zr_adamw_prepare(hp) -> dict:
     h = _hp(hp)
