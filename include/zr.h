@@ -314,15 +314,16 @@ int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const 
  * approximate reciprocal (square root) and exact fma residuals (Markstein's
  * method); this checks that they round as the IEEE operations do. The pages
  * have no counterpart: it is a check of this library's arithmetic.
- *   which 0: sqrt of every float bit pattern in [begin, begin + count);
+ *   which 0: sqrt of every float bit pattern in [begin, begin + count) that
+ *            lies where the kernels take the fma route (+0, [2^-100, FLT_MAX]);
  *         1: reciprocal of every bit pattern in [begin, begin + count) whose
- *            magnitude lies in [2^-60, 2^61) (the range the kernels use it in);
+ *            magnitude lies in [2^-60, 2^60] (the divisors that route sees);
  *         2: count random quotients a / b drawn by splitmix64 from index
- *            begin + i (most inside that range, 1 in 16 any bit pattern),
+ *            begin + i, a = +0 or |a| in [2^-60, 2^61), b in [2^-60, 2^60],
  *            each with a second, near-exact pair a = RN(b q);
- *         3: count random AdamW elements (p, m, v, g over several decades)
- *            under `hp`, compared with the element computed by the IEEE
- *            operations (p, m and v bit for bit).
+ *         3: count random AdamW elements (p, m, v, g over several decades,
+ *            including ones outside that route) under `hp`, compared with the
+ *            element computed by the IEEE operations (p, m and v bit for bit).
  * For which 0 and 1, begin + count <= 2^32. hp is read for which 3 only.
  * Writes the mismatch count to *mismatches and up to min(n_bad, 8) of the
  * offending indices to bad (may be NULL). Allocates a few bytes of device
