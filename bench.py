@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="zr", choices=["zr", "reference"])
     ap.add_argument("--workload", default="irregular_10k")
+    ap.add_argument("--world", type=int, default=0, help="override the workload's emulated replica count")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
@@ -241,7 +242,7 @@ def run_gpu(args, rank, nranks, local, dist):
     from zero_partition_aware_gb300 import workloads as W
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
-    wl = W.WORKLOADS[args.workload]
+    wl = W_lookup(args)
     grp, arenas, table, plan = build_state(wl, device)
     dplan = grp.direct_plan(table)
     L = grp.layout
@@ -420,7 +421,7 @@ def cpu_baseline(wl, budget_s):
 def run_reference(args):
     from zero_partition_aware_gb300 import workloads as W
     import oracle
-    wl = W.WORKLOADS[args.workload]
+    wl = W_lookup(args)
     oracle.build()
     scale = float(np.float32(1.0 / wl.world))
     # each step: a bounded sample (~2 s of single-threaded oracle work)
@@ -464,15 +465,17 @@ def main():
     out = run_gpu(args, rank, nranks, local, dist)
     if rank == 0:
         if nranks == 1 and not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(W_lookup(args.workload), args.cpu_seconds)
+            out["cpu_baseline"] = cpu_baseline(W_lookup(args), args.cpu_seconds)
         print(json.dumps(out), flush=True)
     dist.close()
     return 0
 
 
-def W_lookup(name):
+def W_lookup(args):
+    """The workload named by --workload, with --world applied."""
     from zero_partition_aware_gb300 import workloads as W
-    return W.WORKLOADS[name]
+    wl = W.WORKLOADS[args.workload]
+    return W.replace(wl, world=args.world) if args.world else wl
 
 
 if __name__ == "__main__":

@@ -22,9 +22,15 @@
  *    a message for the calling thread's last failure. The library never
  *    throws across this boundary, never exits or aborts, and its kernels
  *    never trap.
- *  - Device buffers are owned by the caller. The library allocates only the
- *    host-side layout handle (freed by zr_layout_destroy); its kernels use no
- *    scratch memory and take their tables as launch parameters.
+ *  - Device buffers are owned by the caller. The library allocates the
+ *    host-side layout handle (freed by zr_layout_destroy) and, in device
+ *    memory, only the tables of a plan (zr_pack_plan_create,
+ *    zr_direct_plan_create; freed by the matching destroy) and the counters
+ *    of zr_arith_check; the other kernels take their tables as launch
+ *    parameters and use no scratch memory.
+ *  - Kernels may read, never write, bytes that share an aligned 16-byte chunk
+ *    with an element of an input tensor (they move whole aligned chunks);
+ *    such a chunk never crosses a page, so this cannot fault.
  *  - "host array of device pointers": a host array (read during the call
  *    only) whose entries are device addresses.
  *  - Kernels are enqueued on `stream` (NULL = the legacy default stream) and
@@ -277,14 +283,19 @@ int zr_rs_adam_fused(const zr_layout *layout, int64_t bucket, const void *const 
 /*
  * Steps 1 to 4 in one pass, without a bucket buffer. A direct plan records,
  * once, where every replica's gradient of every param of every bucket lives
- * (grads as for zr_bucket_pack; the tensors must stay allocated while the plan
- * is used) and how the bucket positions map to params, in device memory the
- * plan owns (8 bytes per replica and param, plus about 12 bytes per param and
- * 4 per 256 bucket positions). zr_step_direct then does for bucket b what
- * zr_bucket_pack followed by zr_rs_adam_fused does, with identical results:
- * each replica's slice of each param is read where it lies, by its
- * grad_start_offset, instead of being packed first ([DS] §三.2 slicing by
- * param_to_partition_ids / grad_start_offset; [DS] §四). world <= 32.
+ * (grads as for zr_bucket_pack; the tensors must stay allocated, at the same
+ * addresses, while the plan is used) and how the bucket positions map to
+ * params, in device memory the plan owns (8 bytes per replica and param, 8
+ * per param, 36 per 256 bucket positions) plus a host copy of the param
+ * offsets. zr_step_direct then does for bucket b what zr_bucket_pack followed
+ * by zr_rs_adam_fused does, with identical results: each replica's slice of
+ * each param is read where it lies, by its grad_start_offset, instead of
+ * being packed first ([DS] §三.2 slicing by param_to_partition_ids /
+ * grad_start_offset; [DS] §四). One kernel launch per bucket (plus one per
+ * further 2,048 tiles that cross a param boundary, when a bucket has more).
+ * The plan is not modified by zr_step_direct: calls for different buckets
+ * may run on different streams. world <= 32 (ZR_ERR_UNSUPPORTED above).
+ * master, m, v, shard_grad_out, param_bf16: as for zr_rs_adam_fused.
  */
 typedef struct zr_direct_plan zr_direct_plan;
 int zr_direct_plan_create(const zr_layout *layout, const void *const *grads, zr_dtype dtype,
