@@ -107,6 +107,37 @@ class DPGroup:
         for b in range(self.layout.n_buckets):
             self.direct(b, plan, hp, stream=stream)
 
+    def step_direct_from_host(self, plan: zr.DirectPlan, hp, h2d: Sequence[Sequence[tuple]],
+                              param_host: Optional[torch.Tensor] = None, stream=None,
+                              copy_stream=None, d2h_stream=None) -> None:
+        """Every bucket with its gradients arriving from host memory, pipelined
+        over three streams: while bucket b's step runs, bucket b+1's gradients
+        are copied in and bucket b-1's bf16 params are copied out.
+
+        h2d[b]: (host_slice, device_slice) tensor pairs that must be resident
+        before bucket b's step (pinned host memory for asynchronous copies).
+        param_host: pinned bf16 [P] receiving the full parameter buffer, or None.
+        Work is ordered after everything already queued on `stream`, and
+        `stream` waits for all of it at the end."""
+        cur = stream or torch.cuda.current_stream(self.device)
+        cs = copy_stream or torch.cuda.Stream(self.device)
+        ds = d2h_stream or torch.cuda.Stream(self.device)
+        cs.wait_stream(cur)
+        ds.wait_stream(cur)
+        L = self.layout
+        for b in range(L.n_buckets):
+            with torch.cuda.stream(cs):
+                for hs, dv in h2d[b]:
+                    dv.copy_(hs, non_blocking=True)
+            cur.wait_stream(cs)
+            self.direct(b, plan, hp, stream=cur)
+            if param_host is not None:
+                start, n = L.bucket(b)
+                ds.wait_stream(cur)
+                with torch.cuda.stream(ds):
+                    param_host[start:start + n].copy_(self.param[start:start + n], non_blocking=True)
+        cur.wait_stream(ds)
+
     def main_grad_views(self, main_grad: Sequence[torch.Tensor]) -> List[zr.PtrArray]:
         """Per-bucket pointer arrays into flat [P] fp32 per-rank grad buffers: the
         Megatron-style contiguous buffer is already bucket-ordered, so its
