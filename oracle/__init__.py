@@ -71,6 +71,18 @@ _f32 = ctypes.c_float
 def _declare(L):
     L.zro_layout.restype = ctypes.c_int
     L.zro_layout.argtypes = [_vp, _i64, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.zro_layout_ordered.restype = ctypes.c_int
+    L.zro_layout_ordered.argtypes = [_vp, _i64, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.zro_bucket_flat_map.restype = ctypes.c_int
+    L.zro_bucket_flat_map.argtypes = [_vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _vp]
+    L.zro_bucket_pack_ordered.restype = ctypes.c_int
+    L.zro_bucket_pack_ordered.argtypes = [_vp, _i64, _i32, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]
+    L.zro_reduce_scatter_avg_map.restype = ctypes.c_int
+    L.zro_reduce_scatter_avg_map.argtypes = [_i32, _i64, _i64, _vp, _vp, _i32, _f32, _vp]
+    L.zro_rs_adam_fused_map.restype = ctypes.c_int
+    L.zro_rs_adam_fused_map.argtypes = [_i32, _i64, _i64, _i64, _vp, _vp, _i32, _f32,
+                                        _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i64,
+                                        _vp, _vp]
     L.zro_bucket_pack.restype = ctypes.c_int
     L.zro_bucket_pack.argtypes = [_vp, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _i32, _vp]
     L.zro_reduce_scatter_avg.restype = ctypes.c_int
@@ -142,6 +154,9 @@ class Layout:
     bucket_range: np.ndarray   # [nb, 2] flat [start, end)
     slices: np.ndarray         # [ns, 7] param, bucket, dst, param_offset, bucket_offset, partition_offset, numel
     runs: np.ndarray           # [nr, 5] bucket, dst, bucket_offset, partition_offset, numel
+    order: Optional[np.ndarray] = None        # arrival order (None: the flat order)
+    bucket_pos: Optional[np.ndarray] = None   # [n] position of each param in its bucket
+    bucket_info: Optional[np.ndarray] = None  # [nb, 3] numel_b, pad_pos (-1), flat_start (-1)
 
     @property
     def n_params(self) -> int:
@@ -152,8 +167,21 @@ class Layout:
         return int(self.bucket_range.shape[0])
 
     def bucket(self, b: int):
+        """(flat start, numel) of bucket b; the start is -1 when the bucket is not
+        one flat range in flat order (an arrival order other than the flat one)."""
         s, e = (int(x) for x in self.bucket_range[b])
         return s, e - s
+
+    def flat_map(self, b: int) -> np.ndarray:
+        """The flat index of every position of bucket b."""
+        s, nb = self.bucket(b)
+        if self.order is None:
+            return np.arange(s, s + nb, dtype=np.int64)
+        out = np.full(max(nb, 1), -1, dtype=np.int64)
+        _check(lib().zro_bucket_flat_map(_ptr(self.numel), self.n_params, _ptr(self.bucket_of),
+                                         _ptr(self.bucket_pos), b, self.T, int(self.bucket_info[b, 1]),
+                                         self.P, _ptr(out)), "zro_bucket_flat_map")
+        return out[:nb]
 
     def param_partitions(self, i: int):
         """(param_to_partition_ids, grad_start_offset) of param i."""
@@ -164,7 +192,11 @@ class Layout:
         return self.runs[self.runs[:, 0] == b]
 
 
-def layout(numel: Sequence[int], world: int, bucket_size: int) -> Layout:
+def layout(numel: Sequence[int], world: int, bucket_size: int, order: Optional[Sequence[int]] = None) -> Layout:
+    """The layout; `order`: the arrival order of the grads (a permutation of the
+    params; None: the flat order)."""
+    if order is not None:
+        return _layout_ordered(numel, world, bucket_size, order)
     L = lib()
     nm = np.ascontiguousarray(np.asarray(numel, dtype=np.int64))
     n = int(nm.shape[0])
@@ -182,6 +214,30 @@ def layout(numel: Sequence[int], world: int, bucket_size: int) -> Layout:
            "zro_layout(fill)")
     return Layout(nm, world, bucket_size, T, P, S, offset[:n], bucket_of[:n], br[:nb],
                   sl[:ns], ru[:nr])
+
+
+def _layout_ordered(numel, world, bucket_size, order) -> Layout:
+    L = lib()
+    nm = np.ascontiguousarray(np.asarray(numel, dtype=np.int64))
+    od = np.ascontiguousarray(np.asarray(order, dtype=np.int64))
+    n = int(nm.shape[0])
+    assert od.shape == (n,)
+    dims = np.zeros(6, dtype=np.int64)
+    args = (_ptr(nm) if n else None, n, world, bucket_size, _ptr(od) if n else None)
+    _check(L.zro_layout_ordered(*args, _ptr(dims), None, None, None, None, None, None), "zro_layout_ordered(count)")
+    T, P, S, nb, ns, nr = (int(x) for x in dims)
+    offset = np.zeros(max(n, 1), dtype=np.int64)
+    bucket_of = np.zeros(max(n, 1), dtype=np.int64)
+    bucket_pos = np.zeros(max(n, 1), dtype=np.int64)
+    info = np.zeros((max(nb, 1), 3), dtype=np.int64)
+    sl = np.zeros((max(ns, 1), 7), dtype=np.int64)
+    ru = np.zeros((max(nr, 1), 5), dtype=np.int64)
+    _check(L.zro_layout_ordered(*args, _ptr(dims), _ptr(offset), _ptr(bucket_of), _ptr(bucket_pos), _ptr(info),
+                                _ptr(sl), _ptr(ru)), "zro_layout_ordered(fill)")
+    info = info[:nb]
+    br = np.stack([info[:, 2], info[:, 2] + info[:, 0]], axis=1) if nb else np.zeros((0, 2), np.int64)
+    return Layout(nm, world, bucket_size, T, P, S, offset[:n], bucket_of[:n], br, sl[:ns], ru[:nr],
+                  order=od, bucket_pos=bucket_pos[:n], bucket_info=info)
 
 
 # ----------------------------------------------------------------------------
@@ -217,6 +273,12 @@ def bucket_pack(lay: Layout, b: int, grads: Sequence[Sequence[np.ndarray]]) -> L
             assert a.dtype == dt and a.shape == (int(lay.numel[i]),)
             flat.append(np.ascontiguousarray(a))
     ptrs = _ptr_array(flat)
+    if lay.order is not None:
+        pad = int(lay.bucket_info[b, 1])
+        _check(lib().zro_bucket_pack_ordered(_ptr(lay.numel), n, lay.world, _ptr(lay.bucket_of),
+                                             _ptr(lay.bucket_pos), b, pad, lay.P - lay.T, ptrs, es,
+                                             _ptr_array(out)), "zro_bucket_pack_ordered")
+        return out
     _check(lib().zro_bucket_pack(_ptr(lay.numel), _ptr(lay.offset), n, lay.world, lay.T,
                                  start, end, ptrs, es, _ptr_array(out)), "zro_bucket_pack")
     return out
@@ -229,6 +291,11 @@ def reduce_scatter_avg(lay: Layout, b: int, bucket: Sequence[np.ndarray], scale:
     code = _dtype_code(bucket[0])
     for s in shards:
         assert s.dtype == np.float32 and s.shape == (lay.S,)
+    if lay.order is not None:
+        fm = lay.flat_map(b)
+        _check(lib().zro_reduce_scatter_avg_map(lay.world, lay.S, nb, _ptr(fm), _ptr_array(bucket), code,
+                                                scale, _ptr_array(shards)), "zro_reduce_scatter_avg_map")
+        return
     _check(lib().zro_reduce_scatter_avg(lay.world, lay.S, start, nb, _ptr_array(bucket), code,
                                         scale, _ptr_array(shards)), "zro_reduce_scatter_avg")
 
@@ -275,6 +342,15 @@ def rs_adam_fused(lay: Layout, b: int, bucket: Sequence[np.ndarray], scale: floa
                   grad_out: Optional[Sequence[np.ndarray]] = None) -> None:
     start, nb = lay.bucket(b)
     code = _dtype_code(bucket[0])
+    if lay.order is not None:
+        fm = lay.flat_map(b)
+        _check(lib().zro_rs_adam_fused_map(
+            lay.world, lay.T, lay.S, nb, _ptr(fm), _ptr_array(bucket), code, scale,
+            _ptr_array(master), _ptr_array(m), _ptr_array(v),
+            hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step,
+            None if param_bf16 is None else _ptr(param_bf16),
+            None if grad_out is None else _ptr_array(grad_out)), "zro_rs_adam_fused_map")
+        return
     _check(lib().zro_rs_adam_fused(
         lay.world, lay.T, lay.S, start, nb, _ptr_array(bucket), code, scale,
         _ptr_array(master), _ptr_array(m), _ptr_array(v),

@@ -200,6 +200,165 @@ int zro_layout(const int64_t *numel, int64_t n, int32_t world, int64_t bucket_si
     return ZRO_OK;
 }
 
+/*
+ * The same layout when the grads arrive in another order than the flat one:
+ * order[k] is the param whose grad is produced k-th (a permutation of 0..n-1;
+ * backward produces the last layers' grads first, and each grad is copied
+ * into the IPG bucket as soon as it is produced, [DS] §四). The flat layout
+ * and the partitions do not change; only the bucket walk follows arrival:
+ *   - buckets fill in arrival order under the same closing rule;
+ *   - param i sits at bucket_pos[i] in its bucket: the elements of the params
+ *     that arrived before it into the same bucket;
+ *   - the tail padding is reduced with the bucket holding the last flat param
+ *     (n-1), after that bucket's params;
+ *   - a slice's bucket_offset is bucket_pos[i] + (its start - o_i);
+ *   - runs: walking a bucket in bucket order, a slice (or padding piece) is
+ *     merged into the previous piece when they continue each other both in
+ *     the bucket and in the same partition ([DS] §三.2: only contiguous
+ *     fragments aimed at one rank are merged).
+ * With order[k] = k this is zro_layout.
+ * bucket_info[nb][3] = {numel_b, pad_pos (-1: no padding), flat_start (-1
+ * unless the bucket is the flat range [flat_start, flat_start + numel_b) in
+ * order)}; the other outputs as for zro_layout.
+ */
+int zro_layout_ordered(const int64_t *numel, int64_t n, int32_t world, int64_t bucket_size,
+                       const int64_t *order, int64_t *dims, int64_t *offset, int64_t *bucket_of,
+                       int64_t *bucket_pos, int64_t *bucket_info, int64_t *slice, int64_t *run)
+{
+    if (n < 0 || world < 1 || bucket_size < 1) return ZRO_EINVAL;
+    if (n > 0 && (numel == NULL || order == NULL)) return ZRO_EINVAL;
+    int64_t *o = (int64_t *)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+    int64_t *bof = (int64_t *)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+    int64_t *pos = (int64_t *)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+    int64_t *seen = (int64_t *)calloc((size_t)(n > 0 ? n : 1), sizeof(int64_t));
+    if (!o || !bof || !pos || !seen) { free(o); free(bof); free(pos); free(seen); return -3; }
+    int rc = ZRO_OK;
+    for (int64_t k = 0; k < n && rc == ZRO_OK; ++k) {
+        if (numel[k] < 1 || order[k] < 0 || order[k] >= n || seen[order[k]]) rc = ZRO_EINVAL;
+        else seen[order[k]] = 1;
+    }
+    if (rc != ZRO_OK) { free(o); free(bof); free(pos); free(seen); return rc; }
+
+    int64_t T = 0;
+    for (int64_t i = 0; i < n; ++i) { o[i] = T; T += numel[i]; }
+    int64_t P = ((T + world - 1) / world) * world;
+    int64_t S = P / world;
+
+    /* bucket walk in arrival order */
+    int64_t nb = 0, fill = 0;
+    for (int64_t k = 0; k < n; ++k) {
+        int64_t i = order[k];
+        if (k == 0) nb = 1;
+        else if (fill > 0 && fill + numel[i] > bucket_size) { ++nb; fill = 0; }
+        bof[i] = nb - 1;
+        pos[i] = fill;
+        fill += numel[i];
+    }
+    /* each bucket's size, padding position and (when in flat order) flat start */
+    int64_t pad_b = n > 0 ? bof[n - 1] : -1;
+    for (int64_t b = 0; b < nb; ++b) {
+        int64_t size = 0, first = -1, prev = -1, inorder = 1;
+        for (int64_t k = 0; k < n; ++k) {
+            int64_t i = order[k];
+            if (bof[i] != b) continue;
+            size += numel[i];
+            if (first < 0) first = i;
+            else if (i != prev + 1) inorder = 0;
+            prev = i;
+        }
+        int64_t pad_pos = -1;
+        if (b == pad_b) {
+            pad_pos = size;
+            if (prev != n - 1) inorder = 0;
+            size += P - T;
+        }
+        if (bucket_info) {
+            bucket_info[3 * b] = size;
+            bucket_info[3 * b + 1] = pad_pos;
+            bucket_info[3 * b + 2] = inorder ? o[first] : -1;
+        }
+    }
+
+    /* slices, in param order then partition order */
+    int64_t ns = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        for (int64_t r = o[i] / S; r <= (o[i] + numel[i] - 1) / S; ++r) {
+            int64_t lo = max64(o[i], r * S), hi = min64(o[i] + numel[i], (r + 1) * S);
+            if (slice) {
+                int64_t *sl = slice + 7 * ns;
+                sl[0] = i; sl[1] = bof[i]; sl[2] = r; sl[3] = lo - o[i];
+                sl[4] = pos[i] + lo - o[i]; sl[5] = lo - r * S; sl[6] = hi - lo;
+            }
+            ++ns;
+        }
+    }
+
+    /* runs: each bucket in bucket order (its params in arrival order, then the padding) */
+    int64_t nr = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+        int64_t have = 0, pr = -1, px = 0, pp = 0, pn = 0; /* the open piece */
+        for (int64_t k = 0; k <= n; ++k) {
+            /* k < n: the k-th arriving param if it is in b; k == n: the padding if b holds it */
+            int64_t f0, f1, x0;
+            if (k < n) {
+                int64_t i = order[k];
+                if (bof[i] != b) continue;
+                f0 = o[i]; f1 = o[i] + numel[i]; x0 = pos[i];
+            } else {
+                if (b != pad_b || P == T) break;
+                int64_t size_wo_pad = 0;
+                for (int64_t q = 0; q < n; ++q) if (bof[q] == b) size_wo_pad += numel[q];
+                f0 = T; f1 = P; x0 = size_wo_pad;
+            }
+            for (int64_t f = f0; f < f1;) {
+                int64_t r = f / S, hi = min64(f1, (r + 1) * S);
+                int64_t x = x0 + (f - f0), po = f - r * S, len = hi - f;
+                if (have && pr == r && px + pn == x && pp + pn == po) {
+                    pn += len;
+                } else {
+                    if (have) {
+                        if (run) { int64_t *q = run + 5 * nr; q[0] = b; q[1] = pr; q[2] = px; q[3] = pp; q[4] = pn; }
+                        ++nr;
+                    }
+                    have = 1; pr = r; px = x; pp = po; pn = len;
+                }
+                f = hi;
+            }
+        }
+        if (have) {
+            if (run) { int64_t *q = run + 5 * nr; q[0] = b; q[1] = pr; q[2] = px; q[3] = pp; q[4] = pn; }
+            ++nr;
+        }
+    }
+
+    if (offset) memcpy(offset, o, (size_t)n * sizeof(int64_t));
+    if (bucket_of) memcpy(bucket_of, bof, (size_t)n * sizeof(int64_t));
+    if (bucket_pos) memcpy(bucket_pos, pos, (size_t)n * sizeof(int64_t));
+    if (dims) { dims[0] = T; dims[1] = P; dims[2] = S; dims[3] = nb; dims[4] = ns; dims[5] = nr; }
+    free(o); free(bof); free(pos); free(seen);
+    return ZRO_OK;
+}
+
+/*
+ * The flat index of every position of bucket b under an arrival order: param
+ * i's element e sits at bucket position bucket_pos[i] + e and is flat element
+ * o_i + e; padding position pad_pos + j is flat element T + j.
+ */
+int zro_bucket_flat_map(const int64_t *numel, int64_t n, const int64_t *bucket_of, const int64_t *bucket_pos,
+                        int64_t b, int64_t T, int64_t pad_pos, int64_t P, int64_t *flat_of)
+{
+    if (n < 0) return ZRO_EINVAL;
+    int64_t o = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (bucket_of[i] == b)
+            for (int64_t e = 0; e < numel[i]; ++e) flat_of[bucket_pos[i] + e] = o + e;
+        o += numel[i];
+    }
+    if (pad_pos >= 0)
+        for (int64_t j = 0; j < P - T; ++j) flat_of[pad_pos + j] = T + j;
+    return ZRO_OK;
+}
+
 /* ------------------------------------------------------------------------- */
 /* IPG bucket packing                                                          */
 /* ------------------------------------------------------------------------- */
@@ -232,6 +391,32 @@ int zro_bucket_pack(const int64_t *numel, const int64_t *offset, int64_t n, int3
         for (int64_t f = (T > bucket_start ? T : bucket_start); f < bucket_end; ++f)
             for (int32_t c = 0; c < elem_size; ++c)
                 dst[(f - bucket_start) * elem_size + c] = 0;
+    }
+    return ZRO_OK;
+}
+
+/*
+ * The same packing under an arrival order: param i of bucket b lands at its
+ * bucket position bucket_pos[i]; the padding positions [pad_pos, pad_pos +
+ * P - T) of the bucket that holds them are zeroed (pad_pos < 0: none).
+ */
+int zro_bucket_pack_ordered(const int64_t *numel, int64_t n, int32_t world, const int64_t *bucket_of,
+                            const int64_t *bucket_pos, int64_t b, int64_t pad_pos, int64_t pad_n,
+                            const void *const *grads, int32_t elem_size, void *const *out)
+{
+    if (world < 1 || (elem_size != 2 && elem_size != 4) || pad_n < 0) return ZRO_EINVAL;
+    for (int32_t k = 0; k < world; ++k) {
+        unsigned char *dst = (unsigned char *)out[k];
+        for (int64_t i = 0; i < n; ++i) {
+            if (bucket_of[i] != b) continue;
+            const unsigned char *src = (const unsigned char *)grads[(int64_t)k * n + i];
+            for (int64_t e = 0; e < numel[i]; ++e)
+                for (int32_t c = 0; c < elem_size; ++c)
+                    dst[(bucket_pos[i] + e) * elem_size + c] = src[e * elem_size + c];
+        }
+        if (pad_pos >= 0)
+            for (int64_t j = 0; j < pad_n; ++j)
+                for (int32_t c = 0; c < elem_size; ++c) dst[(pad_pos + j) * elem_size + c] = 0;
     }
     return ZRO_OK;
 }
@@ -274,6 +459,20 @@ int zro_reduce_scatter_avg(int32_t world, int64_t S, int64_t bucket_start, int64
     if (world < 1 || S < 1 || numel_b < 0) return ZRO_EINVAL;
     for (int64_t e = 0; e < numel_b; ++e) {
         int64_t f = bucket_start + e;
+        int64_t r = f / S;
+        shard[r][f - r * S] = average_one(world, x, dtype, e, s);
+    }
+    return ZRO_OK;
+}
+
+/* The same for a bucket whose position e holds flat element flat_of[e]
+ * (an arrival order other than the flat one). */
+int zro_reduce_scatter_avg_map(int32_t world, int64_t S, int64_t numel_b, const int64_t *flat_of,
+                               const void *const *x, int32_t dtype, float s, float *const *shard)
+{
+    if (world < 1 || S < 1 || numel_b < 0) return ZRO_EINVAL;
+    for (int64_t e = 0; e < numel_b; ++e) {
+        int64_t f = flat_of[e];
         int64_t r = f / S;
         shard[r][f - r * S] = average_one(world, x, dtype, e, s);
     }
@@ -428,6 +627,27 @@ int zro_rs_adam_fused(int32_t world, int64_t T, int64_t S, int64_t bucket_start,
         if (param_bf16) param_bf16[f] = f < T ? f32_to_bf16(master[r][j]) : (uint16_t)0;
     }
     free(avg);
+    return ZRO_OK;
+}
+
+/* The same for a bucket whose position e holds flat element flat_of[e]. */
+int zro_rs_adam_fused_map(int32_t world, int64_t T, int64_t S, int64_t numel_b, const int64_t *flat_of,
+                          const void *const *x, int32_t dtype, float s,
+                          float *const *master, float *const *m, float *const *v,
+                          float lr, float beta1, float beta2, float eps, float weight_decay, int64_t step,
+                          uint16_t *param_bf16, float *const *grad_out)
+{
+    float c[8];
+    if (world < 1 || S < 1 || numel_b < 0) return ZRO_EINVAL;
+    if (zro_adamw_scalars(lr, beta1, beta2, eps, weight_decay, step, c)) return ZRO_EINVAL;
+    for (int64_t e = 0; e < numel_b; ++e) {
+        float a = average_one(world, x, dtype, e, s);
+        int64_t f = flat_of[e];
+        int64_t r = f / S, j = f - r * S;
+        if (grad_out) grad_out[r][j] = a;
+        adamw_one(c, &master[r][j], &m[r][j], &v[r][j], a);
+        if (param_bf16) param_bf16[f] = f < T ? f32_to_bf16(master[r][j]) : (uint16_t)0;
+    }
     return ZRO_OK;
 }
 
