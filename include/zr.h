@@ -145,6 +145,25 @@ int64_t zr_launch_count(void);
  */
 int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
                      int64_t reduce_bucket_size, zr_layout **out);
+
+/*
+ * The same layout when the grads arrive in another order than the flat one:
+ * arrival[k] is the param whose grad is produced k-th (a permutation of
+ * 0..n_params-1; NULL = the flat order, as zr_layout_create). Backward
+ * produces the last layers' grads first, and each grad is copied into the
+ * IPG bucket as soon as it is produced ([DS] §四), so the buckets fill in
+ * arrival order under the same closing rule; the flat layout and the
+ * partitions do not change. Param i then sits at its own position inside its
+ * bucket (the elements of the params that arrived before it into the same
+ * bucket), the tail padding is reduced with the bucket that holds the last
+ * flat param (after that bucket's params), and a run is a maximal stretch of
+ * a bucket that is also one stretch of one partition ([DS] §三.2: only
+ * contiguous fragments aimed at one rank are merged). Every entry point
+ * below accepts such a layout; results are bit-identical to the flat order's.
+ * ZR_ERR_INVALID_ARG if arrival is not a permutation.
+ */
+int zr_layout_create_ordered(const int64_t *numel, int64_t n_params, int32_t world,
+                             int64_t reduce_bucket_size, const int64_t *arrival, zr_layout **out);
 int zr_layout_destroy(zr_layout *layout);
 int zr_layout_query(const zr_layout *layout, zr_layout_info *info);
 
@@ -152,11 +171,15 @@ int zr_layout_query(const zr_layout *layout, zr_layout_info *info);
  * Writes min(cap, count) entries (either array may be NULL) and the count. */
 int zr_layout_param_partitions(const zr_layout *layout, int64_t param, int32_t *part_ids,
                                int64_t *grad_start_offset, int32_t cap, int32_t *n_out);
-/* All slices (param order, then dst) / runs (bucket order, then dst). Writes
- * min(cap, count) entries (out may be NULL to query the count). */
+/* All slices (param order, then dst) / runs (bucket order, then bucket
+ * offset; in the flat order that is also dst order). Writes min(cap, count)
+ * entries (out may be NULL to query the count). A slice's bucket_offset is
+ * its position in its bucket. */
 int zr_layout_slices(const zr_layout *layout, zr_slice *out, int64_t cap, int64_t *n_out);
 int zr_layout_runs(const zr_layout *layout, zr_run *out, int64_t cap, int64_t *n_out);
-/* Flat start and element count of bucket b. */
+/* Flat start and element count (padding included) of bucket b. The flat
+ * start is -1 when the bucket is not one flat range in flat order (an arrival
+ * order other than the flat one). */
 int zr_layout_bucket(const zr_layout *layout, int64_t b, int64_t *flat_start, int64_t *numel);
 /* Flat offset o_i of param i and the bucket it belongs to. */
 int zr_layout_param(const zr_layout *layout, int64_t param, int64_t *flat_offset, int64_t *bucket);

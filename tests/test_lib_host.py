@@ -68,6 +68,33 @@ def test_layout_matches_oracle_on_workloads(zr, name):
     _same_layout(zr.Layout(list(wl.numel), wl.world, wl.bucket), oracle.layout(list(wl.numel), wl.world, wl.bucket))
 
 
+@pytest.mark.parametrize("seed", range(20))
+def test_ordered_layout_matches_oracle(zr, seed):
+    """Buckets filled in a gradient arrival order (reverse, random, or pairs swapped)."""
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.integers(1, 50))
+    world = int(rng.choice([1, 2, 3, 4, 8, 16, 32]))
+    numel = W.random_numels(rng, n, 1, 6000)
+    B = int(rng.integers(1, 30000))
+    kind = seed % 3
+    if kind == 0:
+        order = list(range(n - 1, -1, -1))
+    elif kind == 1:
+        order = [int(x) for x in rng.permutation(n)]
+    else:
+        order = list(range(n))
+        for i in range(0, n - 1, 2):
+            order[i], order[i + 1] = order[i + 1], order[i]
+    _same_layout(zr.Layout(numel, world, B, arrival=order), oracle.layout(numel, world, B, order=order))
+
+
+def test_ordered_layout_rejects_non_permutations(zr):
+    for bad in ([0, 0, 2], [0, 1, 3], [-1, 1, 2]):
+        with pytest.raises(zr.ZrError) as e:
+            zr.Layout([3, 4, 5], 2, 10, arrival=bad)
+        assert e.value.status == zr.ZR_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("seed", range(30))
 def test_layout_matches_oracle_random(zr, seed):
     rng = np.random.default_rng(seed)

@@ -91,11 +91,18 @@ int zr_version(void) { return 1; }
 // ---------------------------------------------------------------------------
 
 // The flat layout ([DS] §二, [MG] §"分布式优化器"), its buckets ([DS] §四/§五),
-// per-param slices ([DS] §三.2) and per-bucket runs. Runs are computed here as
-// the intersections of each bucket's flat range with the partitions: merging a
-// bucket's same-destination slices (and the padding) gives exactly these.
-int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
-                     int64_t reduce_bucket_size, zr_layout **out) {
+// per-param slices ([DS] §三.2) and per-bucket runs. The buckets fill in the
+// order the grads arrive (the flat order unless `arrival` says otherwise:
+// backward produces the last layers first, and each grad is copied into the
+// IPG bucket as soon as it is produced, [DS] §四); the flat layout and the
+// partitions do not depend on it. A run is a maximal stretch of a bucket that
+// is also one stretch of one partition: walking the bucket in bucket order,
+// a param's piece (or the padding's) joins the previous one when it continues
+// it both in the bucket and in the partition ([DS] §三.2, merging a bucket's
+// same-destination fragments). In flat order the runs are the bucket x
+// partition intersections.
+int zr_layout_create_ordered(const int64_t *numel, int64_t n_params, int32_t world,
+                             int64_t reduce_bucket_size, const int64_t *arrival, zr_layout **out) {
     zr::clear_error();
     if (!out) return fail(ZR_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
@@ -117,49 +124,93 @@ int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
     zr_layout *L = new (std::nothrow) zr_layout();
     if (!L) return fail(ZR_ERR_OOM, "layout handle");
     try {
+        L->arrival.resize(n_params);
+        if (arrival) {
+            std::vector<char> seen(n_params, 0);
+            for (int64_t k = 0; k < n_params; ++k) {
+                const int64_t i = arrival[k];
+                if (i < 0 || i >= n_params || seen[i]) {
+                    delete L;
+                    return fail(ZR_ERR_INVALID_ARG, "arrival is not a permutation of the params (entry %lld)",
+                                (long long)k);
+                }
+                seen[i] = 1;
+                L->arrival[k] = i;
+            }
+        } else {
+            for (int64_t k = 0; k < n_params; ++k) L->arrival[k] = k;
+        }
         L->world = world;
         L->bucket_size = reduce_bucket_size;
         L->T = T;
         L->P = (T + world - 1) / world * world;
         L->S = L->P / world;
+        const int64_t S = L->S;
         L->numel.assign(numel, numel + n_params);
         L->offset.resize(n_params);
         L->bucket_of.resize(n_params);
+        L->bucket_pos.resize(n_params);
         for (int64_t i = 0, o = 0; i < n_params; ++i) {
             L->offset[i] = o;
             o += numel[i];
         }
-        // buckets: [first param, end param) groups, closed before an overflow
-        int64_t i = 0;
-        while (i < n_params) {
-            int64_t j = i, fill = 0;
-            while (j < n_params && (fill == 0 || fill + numel[j] <= reduce_bucket_size)) {
-                fill += numel[j];
+        // buckets: consecutive stretches of the arrival order, closed before an overflow
+        for (int64_t k = 0; k < n_params;) {
+            int64_t j = k, fill = 0;
+            const int64_t b = L->n_buckets();
+            while (j < n_params && (fill == 0 || fill + numel[L->arrival[j]] <= reduce_bucket_size)) {
+                const int64_t i = L->arrival[j];
+                L->bucket_of[i] = b;
+                L->bucket_pos[i] = fill;
+                fill += numel[i];
                 ++j;
             }
-            L->b_param_lo.push_back(i);
-            L->b_param_hi.push_back(j);
-            L->b_start.push_back(L->offset[i]);
-            L->b_end.push_back(j < n_params ? L->offset[j] : L->P);  // last one keeps the padding
-            for (int64_t q = i; q < j; ++q) L->bucket_of[q] = L->n_buckets() - 1;
-            i = j;
+            bool in_order = true;
+            for (int64_t q = k + 1; q < j; ++q) in_order = in_order && L->arrival[q] == L->arrival[q - 1] + 1;
+            L->b_arr_lo.push_back(k);
+            L->b_arr_hi.push_back(j);
+            L->b_size.push_back(fill);
+            L->b_pad_pos.push_back(-1);
+            L->b_flat_start.push_back(in_order ? L->offset[L->arrival[k]] : -1);
+            k = j;
         }
-        const int64_t S = L->S;
-        // runs: bucket x partition intersections, in bucket then rank order
+        if (n_params > 0) {  // the padding travels with the bucket of the last flat param
+            const int64_t pb = L->bucket_of[n_params - 1];
+            L->b_pad_pos[pb] = L->b_size[pb];
+            L->b_size[pb] += L->P - T;
+            if (L->arrival[L->b_arr_hi[pb] - 1] != n_params - 1) L->b_flat_start[pb] = -1;
+        }
+        // runs, bucket by bucket in bucket order
         for (int64_t b = 0; b < L->n_buckets(); ++b) {
             L->b_run_lo.push_back((int64_t)L->runs.size());
-            const int64_t s = L->b_start[b], e = L->b_end[b];
-            for (int64_t r = s / S; r * S < e; ++r) {
-                const int64_t lo = s > r * S ? s : r * S;
-                const int64_t hi = e < (r + 1) * S ? e : (r + 1) * S;
-                zr_run run{};
-                run.bucket = b;
-                run.dst = (int32_t)r;
-                run.bucket_offset = lo - s;
-                run.partition_offset = lo - r * S;
-                run.numel = hi - lo;
-                L->runs.push_back(run);
+            bool open = false;
+            zr_run cur{};
+            auto piece = [&](int64_t f0, int64_t f1, int64_t x0) {
+                for (int64_t f = f0; f < f1;) {
+                    const int64_t r = f / S, hi = f1 < (r + 1) * S ? f1 : (r + 1) * S;
+                    const int64_t x = x0 + (f - f0), po = f - r * S, n = hi - f;
+                    if (open && cur.dst == r && cur.bucket_offset + cur.numel == x &&
+                        cur.partition_offset + cur.numel == po) {
+                        cur.numel += n;
+                    } else {
+                        if (open) L->runs.push_back(cur);
+                        cur = zr_run{};
+                        cur.bucket = b;
+                        cur.dst = (int32_t)r;
+                        cur.bucket_offset = x;
+                        cur.partition_offset = po;
+                        cur.numel = n;
+                        open = true;
+                    }
+                    f = hi;
+                }
+            };
+            for (int64_t k = L->b_arr_lo[b]; k < L->b_arr_hi[b]; ++k) {
+                const int64_t i = L->arrival[k];
+                piece(L->offset[i], L->offset[i] + numel[i], L->bucket_pos[i]);
             }
+            if (L->b_pad_pos[b] >= 0) piece(T, L->P, L->b_pad_pos[b]);
+            if (open) L->runs.push_back(cur);
             L->b_run_hi.push_back((int64_t)L->runs.size());
         }
         // slices: param x partition intersections
@@ -167,7 +218,6 @@ int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
         for (int64_t p = 0; p < n_params; ++p) {
             L->p_slice_lo[p] = (int64_t)L->slices.size();
             const int64_t o = L->offset[p], n = numel[p];
-            const int64_t bs = L->b_start[L->bucket_of[p]];
             for (int64_t r = o / S; r * S < o + n; ++r) {
                 const int64_t lo = o > r * S ? o : r * S;
                 const int64_t hi = o + n < (r + 1) * S ? o + n : (r + 1) * S;
@@ -176,7 +226,7 @@ int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
                 sl.bucket = L->bucket_of[p];
                 sl.dst = (int32_t)r;
                 sl.param_offset = lo - o;
-                sl.bucket_offset = lo - bs;
+                sl.bucket_offset = L->bucket_pos[p] + lo - o;
                 sl.partition_offset = lo - r * S;
                 sl.numel = hi - lo;
                 L->slices.push_back(sl);
@@ -189,6 +239,11 @@ int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
     }
     *out = L;
     return ZR_OK;
+}
+
+int zr_layout_create(const int64_t *numel, int64_t n_params, int32_t world,
+                     int64_t reduce_bucket_size, zr_layout **out) {
+    return zr_layout_create_ordered(numel, n_params, world, reduce_bucket_size, nullptr, out);
 }
 
 int zr_layout_destroy(zr_layout *layout) {
@@ -248,8 +303,8 @@ int zr_layout_bucket(const zr_layout *L, int64_t b, int64_t *flat_start, int64_t
     zr::clear_error();
     if (!L) return fail(ZR_ERR_INVALID_ARG, "NULL layout");
     if (b < 0 || b >= L->n_buckets()) return fail(ZR_ERR_INVALID_ARG, "bucket %lld out of range", (long long)b);
-    if (flat_start) *flat_start = L->b_start[b];
-    if (numel) *numel = L->b_end[b] - L->b_start[b];
+    if (flat_start) *flat_start = L->b_flat_start[b];
+    if (numel) *numel = L->b_size[b];
     return ZR_OK;
 }
 

@@ -15,13 +15,17 @@ struct zr_layout {
     int64_t bucket_size = 1;
     int64_t T = 0, P = 0, S = 0;
     std::vector<int64_t> numel, offset, bucket_of;
-    // per bucket: flat range, param range, run range (runs sorted by bucket then dst)
-    std::vector<int64_t> b_start, b_end, b_param_lo, b_param_hi, b_run_lo, b_run_hi;
-    std::vector<zr_slice> slices;           // param order, then dst
-    std::vector<int64_t> p_slice_lo;        // [n_params + 1] slice index range per param
-    std::vector<zr_run> runs;
+    std::vector<int64_t> arrival;     // the params in the order their grads arrive (fill the buckets)
+    std::vector<int64_t> bucket_pos;  // per param: its position inside its bucket
+    // per bucket: size (padding included), padding position (-1: none), flat
+    // start (-1 unless the bucket is one flat range in flat order), its params
+    // as the index range [b_arr_lo, b_arr_hi) of `arrival`, its runs
+    std::vector<int64_t> b_size, b_pad_pos, b_flat_start, b_arr_lo, b_arr_hi, b_run_lo, b_run_hi;
+    std::vector<zr_slice> slices;     // param order, then dst
+    std::vector<int64_t> p_slice_lo;  // [n_params + 1] slice index range per param
+    std::vector<zr_run> runs;         // bucket order, then bucket position
     int64_t n_params() const { return (int64_t)numel.size(); }
-    int64_t n_buckets() const { return (int64_t)b_start.size(); }
+    int64_t n_buckets() const { return (int64_t)b_size.size(); }
 };
 
 namespace zr {

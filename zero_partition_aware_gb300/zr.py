@@ -81,6 +81,7 @@ _SIGS = {
     "zr_version": (ctypes.c_int, []),
     "zr_launch_count": (ctypes.c_int64, []),
     "zr_layout_create": (ctypes.c_int, [_vp, _i64, _i32, _i64, _P(_vp)]),
+    "zr_layout_create_ordered": (ctypes.c_int, [_vp, _i64, _i32, _i64, _vp, _P(_vp)]),
     "zr_layout_destroy": (ctypes.c_int, [_vp]),
     "zr_layout_query": (ctypes.c_int, [_vp, _P(zr_layout_info)]),
     "zr_layout_param_partitions": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _P(_i32)]),
@@ -211,11 +212,18 @@ class Layout:
     """Owns a zr_layout handle (host memory only)."""
 
     def __init__(self, numel: Sequence[int], world: int,
-                 reduce_bucket_size: int = ZR_DEFAULT_REDUCE_BUCKET_SIZE):
+                 reduce_bucket_size: int = ZR_DEFAULT_REDUCE_BUCKET_SIZE, arrival: Optional[Sequence[int]] = None):
         arr = np.ascontiguousarray(np.asarray(numel, dtype=np.int64))
         h = ctypes.c_void_p()
-        _check(_lib.zr_layout_create(arr.ctypes.data if arr.size else None, int(arr.size), int(world),
-                                     int(reduce_bucket_size), ctypes.byref(h)), "zr_layout_create")
+        if arrival is None:
+            _check(_lib.zr_layout_create(arr.ctypes.data if arr.size else None, int(arr.size), int(world),
+                                         int(reduce_bucket_size), ctypes.byref(h)), "zr_layout_create")
+        else:
+            order = np.ascontiguousarray(np.asarray(arrival, dtype=np.int64))
+            _check(_lib.zr_layout_create_ordered(arr.ctypes.data if arr.size else None, int(arr.size), int(world),
+                                                 int(reduce_bucket_size), order.ctypes.data if order.size else None,
+                                                 ctypes.byref(h)), "zr_layout_create_ordered")
+        self.arrival = None if arrival is None else [int(x) for x in arrival]
         self._h = h
         info = zr_layout_info()
         _check(_lib.zr_layout_query(h, ctypes.byref(info)), "zr_layout_query")
@@ -293,6 +301,11 @@ class Layout:
 
     def offsets(self) -> np.ndarray:
         return np.array([self.param(i)[0] for i in range(self.n_params)], dtype=np.int64)
+
+
+def zr_layout_create_ordered(numel: Sequence[int], world: int, reduce_bucket_size: int,
+                             arrival: Sequence[int]) -> Layout:
+    return Layout(numel, world, reduce_bucket_size, arrival)
 
 
 def zr_layout_create(numel: Sequence[int], world: int,
