@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="zr", choices=["zr", "reference"])
     ap.add_argument("--workload", default="irregular_10k")
     ap.add_argument("--world", type=int, default=0, help="override the workload's emulated replica count")
+    ap.add_argument("--arrival", default="flat", choices=["flat", "reverse"],
+                    help="gradient arrival order that fills the buckets (reverse: backward's order)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
@@ -175,11 +177,12 @@ def profiled_traffic(kernel: str):
 # the GPU arm
 # ----------------------------------------------------------------------------
 
-def build_state(wl, device):
+def build_state(wl, device, arrival="flat"):
     import torch
     from zero_partition_aware_gb300 import workloads as W
     from zero_partition_aware_gb300.engine import DPGroup
-    grp = DPGroup(list(wl.numel), wl.world, wl.bucket, device=device)
+    order = list(range(len(wl.numel) - 1, -1, -1)) if arrival == "reverse" else None
+    grp = DPGroup(list(wl.numel), wl.world, wl.bucket, device=device, arrival=order)
     gen = W.generator(device, 0)
     T = wl.total
     master = torch.randn(T, generator=gen, device=device).mul_(wl.master_std)
@@ -200,8 +203,9 @@ def build_state(wl, device):
 def bucket_bytes(grp, b, world):
     """Algorithmic bytes of the pack and of the fused kernel for bucket b."""
     L = grp.layout
-    start, nb = L.bucket(b)
-    real = max(0, min(start + nb, L.T) - start)  # elements that come from parameter grads
+    _, nb = L.bucket(b)
+    pad = L.P - L.T if L.n_params and L.param(L.n_params - 1)[1] == b else 0
+    real = nb - pad                               # elements that come from parameter grads
     pack = world * (2 * real + 2 * nb)            # read real grads, write the whole bucket
     fused = nb * (2 * world + 12 + 12 + 2)        # N bf16 grads + p,m,v read + p,m,v write + bf16 param
     return pack, fused
@@ -243,7 +247,7 @@ def run_gpu(args, rank, nranks, local, dist):
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
     wl = W_lookup(args)
-    grp, arenas, table, plan = build_state(wl, device)
+    grp, arenas, table, plan = build_state(wl, device, args.arrival)
     dplan = grp.direct_plan(table)
     L = grp.layout
     hp = W.AdamW(step=wl.adam.step)
@@ -312,6 +316,7 @@ def run_gpu(args, rank, nranks, local, dist):
            "config": {"workload": wl.name, "params": L.T, "padded": L.P, "world": wl.world,
                       "reduce_bucket_size": wl.bucket, "buckets": nbk, "grad_dtype": "bf16",
                       "grad_layout": "per-parameter tensors, 512-byte aligned starts",
+                      "arrival": args.arrival,
                       "step": "per bucket: zr_step_direct (pack + reduce-scatter + AdamW + bf16 cast in one pass)",
                       "l2": "no flush: every bucket's working set (~1 GB) exceeds the 129 MB L2",
                       "parallelism": f"replicas only x{nranks}"},

@@ -314,8 +314,9 @@ int zr_rs_adam_fused(const zr_layout *layout, int64_t bucket, const void *const 
  * by zr_rs_adam_fused does, with identical results: each replica's slice of
  * each param is read where it lies, by its grad_start_offset, instead of
  * being packed first ([DS] §三.2 slicing by param_to_partition_ids /
- * grad_start_offset; [DS] §四). One kernel launch per bucket (plus one per
- * further 2,048 tiles that cross a param boundary, when a bucket has more).
+ * grad_start_offset; [DS] §四). One kernel launch per bucket and per 256
+ * runs of it (plus one per further 1,024 tiles that cross a param boundary,
+ * when a launch has more).
  * The plan is not modified by zr_step_direct: calls for different buckets
  * may run on different streams. world <= 32 (ZR_ERR_UNSUPPORTED above).
  * master, m, v, shard_grad_out, param_bf16: as for zr_rs_adam_fused.

@@ -22,8 +22,8 @@ class DPGroup:
     def __init__(self, numel: Sequence[int], world: int,
                  reduce_bucket_size: int = zr.ZR_DEFAULT_REDUCE_BUCKET_SIZE,
                  grad_dtype: torch.dtype = torch.bfloat16, device: str = "cuda",
-                 allocate_buckets: bool = True):
-        self.layout = zr.Layout(numel, world, reduce_bucket_size)
+                 allocate_buckets: bool = True, arrival: Optional[Sequence[int]] = None):
+        self.layout = zr.Layout(numel, world, reduce_bucket_size, arrival=arrival)
         self.world = world
         self.device = torch.device(device)
         self.grad_dtype = grad_dtype
@@ -125,18 +125,44 @@ class DPGroup:
         cs.wait_stream(cur)
         ds.wait_stream(cur)
         L = self.layout
+        spans = self.bucket_flat_spans()
         for b in range(L.n_buckets):
             with torch.cuda.stream(cs):
                 for hs, dv in h2d[b]:
                     dv.copy_(hs, non_blocking=True)
             cur.wait_stream(cs)
             self.direct(b, plan, hp, stream=cur)
-            if param_host is not None:
-                start, n = L.bucket(b)
+            if param_host is not None and spans is not None:
+                lo, hi = spans[b]
                 ds.wait_stream(cur)
                 with torch.cuda.stream(ds):
-                    param_host[start:start + n].copy_(self.param[start:start + n], non_blocking=True)
+                    param_host[lo:hi].copy_(self.param[lo:hi], non_blocking=True)
+        if param_host is not None and spans is None:  # buckets are not flat ranges: copy out at the end
+            ds.wait_stream(cur)
+            with torch.cuda.stream(ds):
+                param_host[: L.P].copy_(self.param[: L.P], non_blocking=True)
         cur.wait_stream(ds)
+
+    def bucket_flat_spans(self):
+        """Per bucket, the flat range [lo, hi) its params (and padding) cover, or
+        None when some bucket's params are not one flat range."""
+        L = self.layout
+        if L.n_buckets == 0:
+            return []
+        lo = [None] * L.n_buckets
+        hi = [0] * L.n_buckets
+        count = [0] * L.n_buckets
+        for i, n in enumerate(L.numel):
+            off, b = L.param(i)
+            lo[b] = off if lo[b] is None else min(lo[b], off)
+            hi[b] = max(hi[b], off + int(n))
+            count[b] += int(n)
+        last = L.param(L.n_params - 1)[1]
+        hi[last] = max(hi[last], L.P)
+        count[last] += L.P - L.T
+        if any(hi[b] - lo[b] != count[b] for b in range(L.n_buckets)):
+            return None
+        return list(zip(lo, hi))
 
     def main_grad_views(self, main_grad: Sequence[torch.Tensor]) -> List[zr.PtrArray]:
         """Per-bucket pointer arrays into flat [P] fp32 per-rank grad buffers: the
