@@ -24,7 +24,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libzr_oracle.so")
 _CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall"]
 
-BF16, FP32 = 0, 1
+BF16, FP32, FP16 = 0, 1, 2
 
 _lib = None
 
@@ -88,7 +88,9 @@ def _declare(L):
     L.zro_reduce_scatter_avg.restype = ctypes.c_int
     L.zro_reduce_scatter_avg.argtypes = [_i32, _i64, _i64, _i64, _vp, _i32, _f32, _vp]
     L.zro_allreduce_avg.restype = ctypes.c_int
-    L.zro_allreduce_avg.argtypes = [_i32, _i64, _vp, _i32, _f32, _vp]
+    L.zro_allreduce_avg.argtypes = [_i32, _i64, _vp, _i32, _f32, _f32, _vp]
+    L.zro_f16_to_f32.restype = None
+    L.zro_f16_to_f32.argtypes = [_vp, _vp, _i64]
     L.zro_grad_accumulate.restype = ctypes.c_int
     L.zro_grad_accumulate.argtypes = [_i64, _vp, _vp, _i32]
     L.zro_adamw_scalars.restype = ctypes.c_int
@@ -134,7 +136,9 @@ def _dtype_code(a: np.ndarray) -> int:
         return BF16
     if a.dtype == np.float32:
         return FP32
-    raise TypeError(f"oracle takes bf16 bit patterns (uint16) or float32, got {a.dtype}")
+    if a.dtype == np.float16:
+        return FP16
+    raise TypeError(f"oracle takes bf16 bit patterns (uint16), float16 or float32, got {a.dtype}")
 
 
 # ----------------------------------------------------------------------------
@@ -300,12 +304,19 @@ def reduce_scatter_avg(lay: Layout, b: int, bucket: Sequence[np.ndarray], scale:
                                         scale, _ptr_array(shards)), "zro_reduce_scatter_avg")
 
 
-def allreduce_avg(world: int, bucket: Sequence[np.ndarray], scale: float) -> List[np.ndarray]:
+def allreduce_avg(world: int, bucket: Sequence[np.ndarray], scale: float, postscale: float = 1.0) -> List[np.ndarray]:
     nb = int(bucket[0].shape[0])
     code = _dtype_code(bucket[0])
     out = [np.empty(nb, dtype=np.float32) for _ in range(world)]
-    _check(lib().zro_allreduce_avg(world, nb, _ptr_array(bucket), code, scale, _ptr_array(out)),
+    _check(lib().zro_allreduce_avg(world, nb, _ptr_array(bucket), code, scale, postscale, _ptr_array(out)),
            "zro_allreduce_avg")
+    return out
+
+
+def f16_to_f32(h: np.ndarray) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.float16)
+    out = np.empty(h.shape, dtype=np.float32)
+    lib().zro_f16_to_f32(_ptr(h), _ptr(out), h.size)
     return out
 
 

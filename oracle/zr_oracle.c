@@ -33,6 +33,7 @@
 
 #define ZRO_BF16 0
 #define ZRO_FP32 1
+#define ZRO_FP16 2
 
 /* ------------------------------------------------------------------------- */
 /* bf16 <-> fp32 by bit pattern                                               */
@@ -62,9 +63,36 @@ static uint16_t f32_to_bf16(float f)
     return (uint16_t)(u >> 16);
 }
 
+/* IEEE 754 binary16 widened to binary32, exactly: sign, 5-bit exponent of
+ * bias 15, 10-bit fraction; exponent 0 holds zero and the subnormals
+ * (fraction x 2^-24), exponent 31 the infinities and NaNs (payload kept).
+ * The fp16 gradients of the pages' fp16 training ([DS] §三.2, §六). */
+static float f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) << 31, e = (h >> 10) & 0x1fu, fr = h & 0x3ffu, u;
+    float f;
+    if (e == 0) {
+        f = ldexpf((float)fr, -24);  /* exact: fr < 2^10 */
+        memcpy(&u, &f, sizeof u);
+        u |= sign;
+    } else if (e == 31) {
+        u = sign | 0x7F800000u | (fr << 13);
+    } else {
+        u = sign | ((e - 15u + 127u) << 23) | (fr << 13);
+    }
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+void zro_f16_to_f32(const uint16_t *in, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = f16_to_f32(in[i]);
+}
+
 static float load_elem(const void *base, int32_t dtype, int64_t i)
 {
     if (dtype == ZRO_BF16) return bf16_to_f32(((const uint16_t *)base)[i]);
+    if (dtype == ZRO_FP16) return f16_to_f32(((const uint16_t *)base)[i]);
     return ((const float *)base)[i];
 }
 
@@ -484,14 +512,18 @@ int zro_reduce_scatter_avg_map(int32_t world, int64_t S, int64_t numel_b, const 
  * is off ([DS] §三.2, gradient_reduction_w_predivide over the whole bucket;
  * [IQ] §"三种原语": every GPU ends with the same full result): every replica k
  * receives the full averaged bucket in out[k], summed in the same order as
- * the reduce-scatter.
+ * the reduce-scatter, then multiplied by `postscale`. That path keeps the
+ * pre- and post-scaling of fp16 training ([DS] §三.2 gradient_predivide_factor
+ * and postscale_gradients; §六: divide before the reduction, scale after):
+ * with predivide factor f, s = 1/f and postscale = f/N; f = N gives
+ * postscale 1, and a product by 1 is exact.
  */
 int zro_allreduce_avg(int32_t world, int64_t numel_b, const void *const *x, int32_t dtype,
-                      float s, float *const *out)
+                      float s, float postscale, float *const *out)
 {
     if (world < 1 || numel_b < 0) return ZRO_EINVAL;
     for (int64_t e = 0; e < numel_b; ++e) {
-        float a = average_one(world, x, dtype, e, s);
+        float a = average_one(world, x, dtype, e, s) * postscale;
         for (int32_t k = 0; k < world; ++k) out[k][e] = a;
     }
     return ZRO_OK;
