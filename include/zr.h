@@ -72,7 +72,10 @@ extern "C" {
 typedef struct CUstream_st *zr_stream; /* the same type as cudaStream_t */
 typedef struct zr_layout zr_layout;    /* opaque, host-owned */
 
-typedef enum { ZR_BF16 = 0, ZR_FP32 = 1 } zr_dtype;
+/* Gradient element types: bf16, fp32, or fp16 (IEEE binary16, the fp16
+ * training the pages' all-reduce path scales for, [DS] §三.2, §六). Every
+ * value is widened to fp32 exactly before any arithmetic. */
+typedef enum { ZR_BF16 = 0, ZR_FP32 = 1, ZR_FP16 = 2 } zr_dtype;
 
 typedef struct {
     int64_t T, P, S;               /* total, padded total, partition size */
@@ -333,11 +336,16 @@ int zr_step_direct(const zr_direct_plan *plan, int64_t bucket, float scale, floa
  * All-reduce with average over one bucket, the path used when
  * reduce_scatter is off ([DS] §三.2 gradient_reduction_w_predivide; [MG]
  * §"四步接力" step 4; [IQ] §"三种原语"): out[k][e] = the same averaged value
- * as zr_reduce_scatter_avg, for every replica k.
+ * as zr_reduce_scatter_avg, then multiplied by `postscale` (fp32, rounded),
+ * for every replica k. That path keeps fp16 training's pre- and post-scaling
+ * ([DS] §三.2 gradient_predivide_factor and postscale_gradients; §六 "divide
+ * first"): with predivide factor f, scale = 1/f and postscale = f/N; f = N
+ * means postscale = 1, which leaves the average unchanged bit for bit.
  * out: host array [world] of device pointers, numel_b fp32 each.
+ * ZR_ERR_INVALID_ARG if postscale is not finite.
  */
 int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
-                     zr_dtype dtype, float scale, float *const *out, zr_stream stream);
+                     zr_dtype dtype, float scale, float postscale, float *const *out, zr_stream stream);
 
 /* ---- arithmetic self-check (device) -------------------------------------- */
 

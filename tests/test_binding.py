@@ -59,7 +59,7 @@ class FakeLib:
     def zr_gather_cast_bf16(self, h, p, param, st):
         return self._rec("cast", p=(p, self.world))
 
-    def zr_allreduce_avg(self, h, b, x, d, s, out, st):
+    def zr_allreduce_avg(self, h, b, x, d, s, post, out, st):
         return self._rec("ar", x=(x, self.world), out=(out, self.world))
 
     def zr_bucket_pack(self, h, b, grads, d, out, st):

@@ -27,7 +27,7 @@ class DPGroup:
         self.world = world
         self.device = torch.device(device)
         self.grad_dtype = grad_dtype
-        self.zr_dtype = zr.ZR_BF16 if grad_dtype == torch.bfloat16 else zr.ZR_FP32
+        self.zr_dtype = {torch.bfloat16: zr.ZR_BF16, torch.float16: zr.ZR_FP16, torch.float32: zr.ZR_FP32}[grad_dtype]
         L = self.layout
         S = L.S
         f32 = dict(dtype=torch.float32, device=self.device)

@@ -27,7 +27,7 @@ ZR_ERR_ALIGN = -4
 ZR_ERR_TIMEOUT = -5
 ZR_ERR_STATE = -6
 ZR_ERR_UNSUPPORTED = -7
-ZR_BF16, ZR_FP32 = 0, 1
+ZR_BF16, ZR_FP32, ZR_FP16 = 0, 1, 2
 ZR_MAX_WORLD = 1024
 ZR_DEFAULT_REDUCE_BUCKET_SIZE = 500_000_000
 ZR_DEFAULT_REDUCE_SCATTER = True
@@ -100,7 +100,7 @@ _SIGS = {
     "zr_gather_cast_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "zr_rs_adam_fused": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp, _vp,
                                         _P(zr_adamw), _vp, _vp, _vp]),
-    "zr_allreduce_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
+    "zr_allreduce_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _f32, _vp, _vp]),
     "zr_direct_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _P(_vp)]),
     "zr_direct_plan_destroy": (ctypes.c_int, [_vp]),
     "zr_step_direct": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
@@ -186,7 +186,9 @@ def _dtype_of(x, dtype) -> int:
             return ZR_BF16
         if seq.dtype == torch.float32:
             return ZR_FP32
-    raise ValueError("cannot infer dtype: pass dtype=ZR_BF16 or ZR_FP32")
+        if seq.dtype == torch.float16:
+            return ZR_FP16
+    raise ValueError("cannot infer dtype: pass dtype=ZR_BF16, ZR_FP32 or ZR_FP16")
 
 
 def _stream(stream) -> int:
@@ -472,11 +474,12 @@ def zr_step_direct(plan: DirectPlan, bucket: int, scale: float, master, m, v, hp
            "zr_step_direct")
 
 
-def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, dtype=None, stream=None) -> None:
+def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, dtype=None, stream=None,
+                     postscale: float = 1.0) -> None:
     d = _dtype_of(bucket_in, dtype)
     px, po = _ptrs(bucket_in), _ptrs(out)
-    _check(_lib.zr_allreduce_avg(layout.handle, int(bucket), px.ptr, d, float(scale), po.ptr, _stream(stream)),
-           "zr_allreduce_avg")
+    _check(_lib.zr_allreduce_avg(layout.handle, int(bucket), px.ptr, d, float(scale), float(postscale), po.ptr,
+                                 _stream(stream)), "zr_allreduce_avg")
 
 
 # ----------------------------------------------------------------------------
