@@ -14,7 +14,7 @@ import ctypes
 import os
 import subprocess
 from dataclasses import dataclass
-from typing import List, Optional, Sequence
+from typing import List, NamedTuple, Optional, Sequence
 
 import numpy as np
 
@@ -103,6 +103,11 @@ def _declare(L):
     L.zro_rs_adam_fused.argtypes = [_i32, _i64, _i64, _i64, _i64, _vp, _i32, _f32,
                                     _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i64,
                                     _vp, _vp]
+    L.zro_grad_check.restype = ctypes.c_int
+    L.zro_grad_check.argtypes = [_i32, _i64, _vp, _f32, _vp, _vp, _vp, _vp, _vp]
+    L.zro_adam_clip_step.restype = ctypes.c_int
+    L.zro_adam_clip_step.argtypes = [_i32, _i64, _i64, _vp, _vp, _vp, _vp, _f32, _i32,
+                                     _f32, _f32, _f32, _f32, _f32, _i64, _vp]
     L.zro_comm_bytes.restype = ctypes.c_int
     L.zro_comm_bytes.argtypes = [_i32, _i32, _i64, _i32, ctypes.POINTER(ctypes.c_double)]
     L.zro_layout_bytes.restype = ctypes.c_int
@@ -368,6 +373,38 @@ def rs_adam_fused(lay: Layout, b: int, bucket: Sequence[np.ndarray], scale: floa
         hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step,
         None if param_bf16 is None else _ptr(param_bf16),
         None if grad_out is None else _ptr_array(grad_out)), "zro_rs_adam_fused")
+
+
+class GradStats(NamedTuple):
+    """The global gradient check's outcome (zro_grad_check)."""
+    sumsq: float
+    nonfinite: int
+    norm: float
+    coef: float
+    skip: bool
+
+
+def grad_check(grad: Sequence[np.ndarray], max_norm: float) -> GradStats:
+    """Global L2 norm, overflow count and clip coefficient of every rank's averaged shard."""
+    S = grad[0].size
+    for a in grad:
+        assert a.dtype == np.float32 and a.size == S
+    sumsq, norm = ctypes.c_double(), ctypes.c_double()
+    bad, skip, coef = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_float()
+    _check(lib().zro_grad_check(len(grad), S, _ptr_array(grad), max_norm, ctypes.byref(sumsq), ctypes.byref(bad),
+                                ctypes.byref(norm), ctypes.byref(coef), ctypes.byref(skip)), "zro_grad_check")
+    return GradStats(sumsq.value, bad.value, norm.value, coef.value, bool(skip.value))
+
+
+def adam_clip_step(lay: Layout, master, m, v, grad, hp, coef: float, skip: bool,
+                   param_bf16: Optional[np.ndarray] = None) -> None:
+    """The step the check steers: nothing if skip, else AdamW on g * coef and the bf16 cast."""
+    for arrs in (master, m, v, grad):
+        assert len(arrs) == lay.world and all(a.dtype == np.float32 and a.size == lay.S for a in arrs)
+    _check(lib().zro_adam_clip_step(
+        lay.world, lay.T, lay.S, _ptr_array(master), _ptr_array(m), _ptr_array(v), _ptr_array(grad),
+        coef, int(skip), hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step,
+        None if param_bf16 is None else _ptr(param_bf16)), "zro_adam_clip_step")
 
 
 def comm_bytes(scheme: int, world: int, S: int, elem_bytes: int) -> float:

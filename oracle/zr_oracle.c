@@ -684,6 +684,89 @@ int zro_rs_adam_fused_map(int32_t world, int64_t T, int64_t S, int64_t numel_b, 
 }
 
 /* ------------------------------------------------------------------------- */
+/* Global gradient check before the step, and the step it steers               */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Runs once every bucket has been averaged into the partitions and before
+ * the optimizer step ([MG] §"跨 model-parallel 的梯度收尾": DP sync first,
+ * then the remaining gradient fix-ups, then optimizer.step(); [DS] §六: fp16
+ * training guards the gradient arithmetic). The pages give no formula, so
+ * this is the usual one:
+ *   sumsq     = sum over r = 0..N-1, j = 0..S-1 (flat order) of g[r][j]^2,
+ *               each square exact in double (a 24-bit significand squared
+ *               fits in 53 bits), summed in double;
+ *   norm      = sqrt(sumsq), in double (the global L2 norm of the averaged
+ *               gradient over every rank's partition);
+ *   nonfinite = the number of elements whose fp32 square g*g is not finite
+ *               (NaN, an infinity, or |g| so large that its square
+ *               overflows fp32);
+ *   skip      = nonfinite > 0: the step changes nothing (an overflowed
+ *               step is dropped, as fp16 loss scaling does);
+ *   coef      = fp32(min(1, max_norm / (norm + 1e-6))), computed in double
+ *               and rounded once, when max_norm > 0 and skip == 0; else 1
+ *               (gradient clipping by the global norm).
+ * g[r] is rank r's averaged shard gradient (S fp32).
+ */
+int zro_grad_check(int32_t world, int64_t S, const float *const *g, float max_norm,
+                   double *sumsq, int64_t *nonfinite, double *norm, float *coef, int32_t *skip)
+{
+    if (world < 1 || S < 0) return ZRO_EINVAL;
+    double acc = 0.0;
+    int64_t bad = 0;
+    for (int32_t r = 0; r < world; ++r)
+        for (int64_t j = 0; j < S; ++j) {
+            float x = g[r][j];
+            float sq32 = x * x;
+            if (!isfinite(sq32)) ++bad;
+            double d = (double)x;
+            acc = acc + d * d;
+        }
+    double nrm = sqrt(acc);
+    float c = 1.0f;
+    if (max_norm > 0.0f && bad == 0) {
+        double q = (double)max_norm / (nrm + 1e-6);
+        c = q < 1.0 ? (float)q : 1.0f;
+    }
+    *sumsq = acc;
+    *nonfinite = bad;
+    *norm = nrm;
+    *coef = c;
+    *skip = bad > 0;
+    return ZRO_OK;
+}
+
+/*
+ * The step the check steers, over every rank's shard: if skip, nothing is
+ * written. Otherwise, for every rank r and shard element j:
+ *   gc = g[r][j] * coef (fp32, rounded; exact when coef = 1),
+ *   AdamW on master[r][j], m[r][j], v[r][j] with gc (adamw_one above),
+ *   param_bf16[rS + j] = bf16(master[r][j]) for rS + j < T, 0 for the padding
+ * ([MG] §"通信模式": the fp32 update of the local slice, then the
+ * all-gather's payload). param_bf16 may be NULL.
+ */
+int zro_adam_clip_step(int32_t world, int64_t T, int64_t S, float *const *master, float *const *m,
+                       float *const *v, const float *const *g, float coef, int32_t skip,
+                       float lr, float beta1, float beta2, float eps, float weight_decay, int64_t step,
+                       uint16_t *param_bf16)
+{
+    float c[8];
+    if (world < 1 || S < 0) return ZRO_EINVAL;
+    if (zro_adamw_scalars(lr, beta1, beta2, eps, weight_decay, step, c)) return ZRO_EINVAL;
+    if (skip) return ZRO_OK;
+    for (int32_t r = 0; r < world; ++r)
+        for (int64_t j = 0; j < S; ++j) {
+            float gc = g[r][j] * coef;
+            adamw_one(c, &master[r][j], &m[r][j], &v[r][j], gc);
+            if (param_bf16) {
+                int64_t f = (int64_t)r * S + j;
+                param_bf16[f] = f < T ? f32_to_bf16(master[r][j]) : (uint16_t)0;
+            }
+        }
+    return ZRO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Byte accounting                                                             */
 /* ------------------------------------------------------------------------- */
 
