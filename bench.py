@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--world", type=int, default=0, help="override the workload's emulated replica count")
     ap.add_argument("--arrival", default="flat", choices=["flat", "reverse"],
                     help="gradient arrival order that fills the buckets (reverse: backward's order)")
+    ap.add_argument("--max-norm", type=float, default=1.0,
+                    help="clip norm of the step with the global gradient check (<= 0: check without clipping)")
+    ap.add_argument("--no-clipped", action="store_true", help="skip timing the step with the gradient check")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
@@ -241,6 +244,40 @@ def timed_steps(args, nbk, launch_a, launch_b, stream, dist):
     return ms_step, t_a, t_b, launches
 
 
+def timed_clipped(args, grp, dplan, hp, stream, dist):
+    """K steps of the two-pass step with the global gradient check: every
+    bucket averaged into the gradient partitions with the norm sums, then the
+    check and the clipped AdamW + cast. CUDA events around the norm pass, the
+    check and the update. Returns (ms/step, norm ms, check ms, update ms,
+    launches, the last outcome)."""
+    import torch
+    from zero_partition_aware_gb300 import zr
+    nbk = grp.layout.n_buckets
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    n0 = zr.zr_launch_count()
+    start_ev.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        for b in range(nbk):
+            zr.zr_rs_direct_norm(dplan, b, grp.scale, grp._p_grad, grp.check, stream=stream)
+        ev[k][1].record(stream)
+        zr.zr_grad_check_finalize(grp.check, args.max_norm, stream=stream)
+        ev[k][2].record(stream)
+        zr.zr_adam_clip_step(grp.layout, grp._p_master, grp._p_m, grp._p_v, grp._p_grad, hp, grp.check,
+                             grp.param, stream=stream)
+        ev[k][3].record(stream)
+    end_ev.record(stream)
+    torch.cuda.synchronize()
+    launches = zr.zr_launch_count() - n0
+    dist.barrier()
+    t = [sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) for i in range(3)]
+    ms_step = dist.max(start_ev.elapsed_time(end_ev) / args.steps)
+    return ms_step, t[0], t[1], t[2], launches, zr.zr_gradcheck_read(grp.check, stream)
+
+
 def run_gpu(args, rank, nranks, local, dist):
     import torch
     from zero_partition_aware_gb300 import workloads as W
@@ -306,6 +343,30 @@ def run_gpu(args, rank, nranks, local, dist):
                           "frac_of_peak": round(fused_gbs / peak, 4), "bytes_per_param": 2 * wl.world + 26},
     }
 
+    clipped = None
+    if not args.no_clipped:
+        # the step with the global gradient check before the update (two passes)
+        grp.grad_shards()
+        for _ in range(W_):
+            grp.step_direct_clipped(dplan, hp, args.max_norm, stream=stream)
+        torch.cuda.synchronize()
+        ms_c, t_norm, t_fin, t_clip, launches_c, outcome = timed_clipped(args, grp, dplan, hp, stream, dist)
+        norm_bytes = L.P * (2 * wl.world + 4)
+        clip_bytes = L.P * 30
+        clipped = {
+            "ms_per_step": round(ms_c, 4), "params_per_s": round(nranks * L.T / (ms_c / 1e3)),
+            "max_norm": args.max_norm, "launches_per_step": round(launches_c / args.steps),
+            "outcome": {"norm": outcome["norm"], "coef": outcome["coef"], "skip": outcome["skip"]},
+            "rs_direct_norm": {"ms_per_step": round(t_norm / args.steps, 4),
+                               "GB_per_s": round(gbs(norm_bytes, t_norm), 1),
+                               "frac_of_peak": round(gbs(norm_bytes, t_norm) / peak, 4),
+                               "bytes_per_param": 2 * wl.world + 4},
+            "grad_check_finalize": {"ms_per_step": round(t_fin / args.steps, 4)},
+            "adam_clip_step": {"ms_per_step": round(t_clip / args.steps, 4),
+                               "GB_per_s": round(gbs(clip_bytes, t_clip), 1),
+                               "frac_of_peak": round(gbs(clip_bytes, t_clip) / peak, 4), "bytes_per_param": 30},
+        }
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, grp, arenas, dplan, hp, stream, nranks, dist)
@@ -322,6 +383,8 @@ def run_gpu(args, rank, nranks, local, dist):
                       "parallelism": f"replicas only x{nranks}"},
            "roofline": roofline, "kernels": kernels, "two_kernel_step": two_kernel,
            "gpu_launches": int(launches), "clocks": clk}
+    if clipped is not None:
+        out["clipped_step"] = clipped
     if e2e is not None:
         out["e2e"] = e2e
     return out

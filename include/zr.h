@@ -25,8 +25,9 @@
  *  - Device buffers are owned by the caller. The library allocates the
  *    host-side layout handle (freed by zr_layout_destroy) and, in device
  *    memory, only the tables of a plan (zr_pack_plan_create,
- *    zr_direct_plan_create; freed by the matching destroy) and the counters
- *    of zr_arith_check; the other kernels take their tables as launch
+ *    zr_direct_plan_create; freed by the matching destroy), the sums of a
+ *    gradient check (zr_gradcheck_create) and the counters of
+ *    zr_arith_check; the other kernels take their tables as launch
  *    parameters and use no scratch memory.
  *  - Kernels may read, never write, bytes that share an aligned 16-byte chunk
  *    with an element of an input tensor (they move whole aligned chunks);
@@ -346,6 +347,97 @@ int zr_step_direct(const zr_direct_plan *plan, int64_t bucket, float scale, floa
  */
 int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
                      zr_dtype dtype, float scale, float postscale, float *const *out, zr_stream stream);
+
+/* ---- global gradient check before the step -------------------------------- */
+
+/*
+ * Between the DP sync of every bucket and optimizer.step() ([MG]
+ * §"跨 model-parallel 的梯度收尾": DP sync first, then the remaining gradient
+ * fix-ups, then the step; [DS] §六: fp16 training guards its gradient
+ * arithmetic): the global L2 norm of the averaged gradient over every rank's
+ * partition, an overflow check, and clipping by that norm. The pages give no
+ * formula; the usual one is taken:
+ *   sumsq     = the sum of g^2 over every rank's shard gradient;
+ *   norm      = sqrt(sumsq);
+ *   nonfinite = the number of elements whose fp32 square g*g is not finite;
+ *   skip      = nonfinite > 0: the step changes nothing (an overflowed step
+ *               is dropped, as fp16 loss scaling does; the loss scale is
+ *               the caller's, and 1/loss_scale may be folded into `scale`);
+ *   coef      = fp32(min(1, max_norm / (norm + 1e-6))) when max_norm > 0
+ *               and not skip, else 1.
+ * The check needs the whole gradient before any element's update, so the
+ * step takes two passes: the averaging of every bucket into the shard
+ * gradients (zr_rs_direct_norm or zr_reduce_scatter_avg_norm, which also add
+ * to the check's sums), then zr_grad_check_finalize and zr_adam_clip_step.
+ * The outcome stays in device memory (no host round trip) until
+ * zr_gradcheck_read.
+ *
+ * Accuracy: a thread adds the fp32 squares of its 8 elements of a tile in
+ * fp32 and the result to a double (a square outside [2^-100, 2^100] goes to
+ * the double exactly), so sumsq is within about 1e-6 relative of the exact
+ * sum. The blocks' sums are added in a fixed order, so the outcome repeats
+ * exactly for the same inputs and launch sequence on the same device when
+ * the calls that add to one check are ordered (one stream, or events);
+ * concurrent calls still add correctly, in some order.
+ */
+typedef struct {
+    double sumsq;        /* the sum of squares */
+    double norm;         /* sqrt(sumsq) */
+    uint64_t nonfinite;  /* averaged gradients whose fp32 square is not finite */
+    float coef;          /* the clip coefficient the step applies */
+    int32_t skip;        /* 1: the step leaves every state unchanged */
+} zr_grad_stats;
+
+typedef struct zr_gradcheck zr_gradcheck;
+
+/* Allocates on the current device the check's sums (32 KB, zeroed) and its
+ * outcome (coef = 1, skip = 0 until the first finalize). */
+int zr_gradcheck_create(zr_gradcheck **out);
+int zr_gradcheck_destroy(zr_gradcheck *chk);
+
+/* Clears the sums (after a step abandoned before its finalize). */
+int zr_gradcheck_reset(zr_gradcheck *chk, zr_stream stream);
+
+/*
+ * zr_reduce_scatter_avg over one packed bucket, also adding the averages'
+ * squares and non-finite count to chk.
+ */
+int zr_reduce_scatter_avg_norm(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
+                               zr_dtype dtype, float scale, float *const *shard_grad, zr_gradcheck *chk,
+                               zr_stream stream);
+
+/*
+ * The direct plan's pass without the optimizer: every replica's gradients of
+ * bucket b, read where they lie, averaged into shard_grad exactly as
+ * zr_bucket_pack followed by zr_reduce_scatter_avg would, adding to chk.
+ * shard_grad: host array [world] of device pointers, S fp32 each (the
+ * entries of the ranks the bucket intersects). world <= 32.
+ */
+int zr_rs_direct_norm(const zr_direct_plan *plan, int64_t bucket, float scale, float *const *shard_grad,
+                      zr_gradcheck *chk, zr_stream stream);
+
+/*
+ * Once every bucket has been added: sums chk's accumulators in a fixed
+ * order, writes the outcome for max_norm (<= 0: no clipping; NaN is
+ * ZR_ERR_INVALID_ARG) and clears the accumulators for the next step.
+ */
+int zr_grad_check_finalize(zr_gradcheck *chk, float max_norm, zr_stream stream);
+
+/*
+ * The step the outcome steers, over every rank's shard: nothing if skip;
+ * otherwise for every element, gc = grad * coef (fp32, exact when coef = 1),
+ * the AdamW update of zr_adam_shard_step with gc, and the bf16 cast of
+ * zr_gather_cast_bf16 into param_bf16 ([MG] §"通信模式"). With max_norm <= 0
+ * and finite gradients the results equal those of zr_rs_adam_fused bit for
+ * bit. master, m, v (in/out) and grad: host arrays [world] of device
+ * pointers, S fp32 each. param_bf16: device [P] bf16 or NULL.
+ */
+int zr_adam_clip_step(const zr_layout *layout, float *const *master, float *const *m, float *const *v,
+                      const float *const *grad, const zr_adamw *hp, const zr_gradcheck *chk,
+                      void *param_bf16, zr_stream stream);
+
+/* Waits for `stream`, then copies the last finalized outcome to *out. */
+int zr_gradcheck_read(const zr_gradcheck *chk, zr_stream stream, zr_grad_stats *out);
 
 /* ---- arithmetic self-check (device) -------------------------------------- */
 

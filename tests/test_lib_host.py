@@ -207,3 +207,37 @@ def test_launch_without_device_reports_state(zr):
     two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
     rc = zr._lib.zr_reduce_scatter_avg(lay.handle, 0, two, zr.ZR_BF16, 0.5, two, None)
     assert rc in (zr.ZR_ERR_STATE, zr.ZR_ERR_CUDA)
+
+
+def test_gradient_check_validates_before_launch(zr):
+    """The global gradient check's entry points reject bad arguments on the host."""
+    lay = zr.Layout([100, 200], 2, 1000)
+    L = zr._lib
+    two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    odd = (ctypes.c_void_p * 2)(0x1001, 0x2000)
+    hp = zr.zr_adamw(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)
+    assert L.zr_gradcheck_create(None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_gradcheck_destroy(None) == zr.ZR_OK
+    assert L.zr_gradcheck_reset(None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_grad_check_finalize(None, 1.0, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_gradcheck_read(None, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_rs_direct_norm(None, 0, 0.5, two, None, None) == zr.ZR_ERR_INVALID_ARG
+    # the layout and pointer checks come before the check object's
+    assert L.zr_reduce_scatter_avg_norm(lay.handle, 0, odd, zr.ZR_BF16, 0.5, two, None, None) == zr.ZR_ERR_ALIGN
+    assert L.zr_reduce_scatter_avg_norm(lay.handle, 5, two, zr.ZR_BF16, 0.5, two, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_reduce_scatter_avg_norm(lay.handle, 0, two, zr.ZR_BF16, 0.5, two, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_adam_clip_step(None, two, two, two, two, ctypes.byref(hp), None, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_adam_clip_step(lay.handle, two, two, two, None, ctypes.byref(hp), None, None,
+                               None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_adam_clip_step(lay.handle, two, two, two, two, ctypes.byref(hp), None, None,
+                               None) == zr.ZR_ERR_INVALID_ARG
+    assert "gradient check" in zr.last_error()
+
+
+def test_gradient_check_create_without_device_reports_state(zr):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: this check only runs on a machine without one")
+    h = ctypes.c_void_p()
+    assert zr._lib.zr_gradcheck_create(ctypes.byref(h)) in (zr.ZR_ERR_STATE, zr.ZR_ERR_OOM, zr.ZR_ERR_CUDA)
+    assert not h.value

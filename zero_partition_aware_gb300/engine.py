@@ -107,6 +107,50 @@ class DPGroup:
         for b in range(self.layout.n_buckets):
             self.direct(b, plan, hp, stream=stream)
 
+    # ---- the step with a global gradient check ---------------------------------------
+    def grad_shards(self) -> List[torch.Tensor]:
+        """Each rank's fp32 averaged-gradient partition (S elements), allocated on
+        first use: the two-pass step keeps the whole averaged gradient until
+        the check has seen all of it (the partition gradient of stage 2)."""
+        if getattr(self, "_grad", None) is None:
+            self._grad = [torch.zeros(self.layout.S, dtype=torch.float32, device=self.device)
+                          for _ in range(self.world)]
+            self._p_grad = zr.PtrArray(self._grad)
+            self.check = zr.GradCheck()
+        return self._grad
+
+    def step_direct_clipped(self, plan: zr.DirectPlan, hp, max_norm: float, stream=None) -> None:
+        """The step with the global gradient check before the update ("Megatron-LM
+        分布式训练（四）" §"跨 model-parallel 的梯度收尾": DP sync, then the gradient
+        fix-ups, then optimizer.step()): every bucket averaged into the
+        gradient partitions while the norm is summed, the check (norm,
+        overflow, clip coefficient for max_norm; <= 0 disables clipping), then
+        the clipped AdamW + bf16 cast over every partition, or nothing when
+        the check found an overflow. The outcome stays on the device
+        (``zr.zr_gradcheck_read(self.check)`` reads it)."""
+        self.grad_shards()
+        for b in range(self.layout.n_buckets):
+            zr.zr_rs_direct_norm(plan, b, self.scale, self._p_grad, self.check, stream=stream)
+        self.finish_clipped(hp, max_norm, stream)
+
+    def step_clipped(self, grad_table: zr.PtrArray, hp, max_norm: float, stream=None,
+                     plan: Optional[zr.PackPlan] = None) -> None:
+        """The same from packed buckets: pack, then the averaging with the norm."""
+        self.grad_shards()
+        for b in range(self.layout.n_buckets):
+            if plan is not None:
+                self.pack_planned(b, plan, stream)
+            else:
+                self.pack(b, grad_table, stream)
+            zr.zr_reduce_scatter_avg_norm(self.layout, b, self._p_buckets, self.scale, self._p_grad, self.check,
+                                          dtype=self.zr_dtype, stream=stream)
+        self.finish_clipped(hp, max_norm, stream)
+
+    def finish_clipped(self, hp, max_norm: float, stream=None) -> None:
+        zr.zr_grad_check_finalize(self.check, max_norm, stream=stream)
+        zr.zr_adam_clip_step(self.layout, self._p_master, self._p_m, self._p_v, self._p_grad, hp, self.check,
+                             self.param, stream=stream)
+
     def step_direct_from_host(self, plan: zr.DirectPlan, hp, h2d: Sequence[Sequence[tuple]],
                               param_host: Optional[torch.Tensor] = None, stream=None,
                               copy_stream=None, d2h_stream=None) -> None:

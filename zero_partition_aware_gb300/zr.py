@@ -66,6 +66,11 @@ class zr_adamw(ctypes.Structure):
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
 
 
+class zr_grad_stats(ctypes.Structure):
+    _fields_ = [("sumsq", ctypes.c_double), ("norm", ctypes.c_double), ("nonfinite", ctypes.c_uint64),
+                ("coef", ctypes.c_float), ("skip", ctypes.c_int32)]
+
+
 class zr_adamw_scalars(ctypes.Structure):
     _fields_ = [(n, ctypes.c_float) for n in ("beta1", "one_minus_beta1", "beta2", "one_minus_beta2",
                                                 "step_size", "bc2_sqrt", "decay", "eps")]
@@ -104,6 +109,14 @@ _SIGS = {
     "zr_direct_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _P(_vp)]),
     "zr_direct_plan_destroy": (ctypes.c_int, [_vp]),
     "zr_step_direct": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
+    "zr_gradcheck_create": (ctypes.c_int, [_P(_vp)]),
+    "zr_gradcheck_destroy": (ctypes.c_int, [_vp]),
+    "zr_gradcheck_reset": (ctypes.c_int, [_vp, _vp]),
+    "zr_reduce_scatter_avg_norm": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp, _vp]),
+    "zr_rs_direct_norm": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp]),
+    "zr_grad_check_finalize": (ctypes.c_int, [_vp, _f32, _vp]),
+    "zr_adam_clip_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
+    "zr_gradcheck_read": (ctypes.c_int, [_vp, _vp, _P(zr_grad_stats)]),
     "zr_adamw_prepare": (ctypes.c_int, [_P(zr_adamw), _P(zr_adamw_scalars)]),
     "zr_arith_check": (ctypes.c_int, [_i32, ctypes.c_uint64, ctypes.c_uint64, _P(zr_adamw),
                                       _P(ctypes.c_uint64), _P(ctypes.c_uint64), _i32]),
@@ -480,6 +493,77 @@ def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, 
     px, po = _ptrs(bucket_in), _ptrs(out)
     _check(_lib.zr_allreduce_avg(layout.handle, int(bucket), px.ptr, d, float(scale), float(postscale), po.ptr,
                                  _stream(stream)), "zr_allreduce_avg")
+
+
+class GradCheck:
+    """Owns a zr_gradcheck: the device-side sums and outcome of the global
+    gradient check (norm, overflow, clip coefficient) between the averaging
+    of every bucket and the optimizer step."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        _check(_lib.zr_gradcheck_create(ctypes.byref(h)), "zr_gradcheck_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.zr_gradcheck_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def zr_gradcheck_create() -> GradCheck:
+    return GradCheck()
+
+
+def zr_gradcheck_destroy(chk: GradCheck) -> None:
+    chk.close()
+
+
+def zr_gradcheck_reset(chk: GradCheck, stream=None) -> None:
+    _check(_lib.zr_gradcheck_reset(chk.handle, _stream(stream)), "zr_gradcheck_reset")
+
+
+def zr_reduce_scatter_avg_norm(layout: Layout, bucket: int, bucket_in, scale: float, shard_grad, chk: GradCheck,
+                               dtype=None, stream=None) -> None:
+    d = _dtype_of(bucket_in, dtype)
+    x, g = _ptrs(bucket_in), _ptrs(shard_grad)
+    _check(_lib.zr_reduce_scatter_avg_norm(layout.handle, int(bucket), x.ptr, d, float(scale), g.ptr, chk.handle,
+                                           _stream(stream)), "zr_reduce_scatter_avg_norm")
+
+
+def zr_rs_direct_norm(plan: DirectPlan, bucket: int, scale: float, shard_grad, chk: GradCheck, stream=None) -> None:
+    g = _ptrs(shard_grad)
+    _check(_lib.zr_rs_direct_norm(plan.handle, int(bucket), float(scale), g.ptr, chk.handle, _stream(stream)),
+           "zr_rs_direct_norm")
+
+
+def zr_grad_check_finalize(chk: GradCheck, max_norm: float, stream=None) -> None:
+    _check(_lib.zr_grad_check_finalize(chk.handle, float(max_norm), _stream(stream)), "zr_grad_check_finalize")
+
+
+def zr_adam_clip_step(layout: Layout, master, m, v, grad, hp, chk: GradCheck, param_bf16=None, stream=None) -> None:
+    h = _hp(hp)
+    pm, pmm, pv, pg = _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(grad)
+    _check(_lib.zr_adam_clip_step(layout.handle, pm.ptr, pmm.ptr, pv.ptr, pg.ptr, ctypes.byref(h), chk.handle,
+                                  _addr(param_bf16), _stream(stream)), "zr_adam_clip_step")
+
+
+def zr_gradcheck_read(chk: GradCheck, stream=None) -> dict:
+    """The last finalized outcome (waits for the stream)."""
+    st = zr_grad_stats()
+    _check(_lib.zr_gradcheck_read(chk.handle, _stream(stream), ctypes.byref(st)), "zr_gradcheck_read")
+    return {"sumsq": st.sumsq, "norm": st.norm, "nonfinite": int(st.nonfinite), "coef": st.coef,
+            "skip": bool(st.skip)}
 
 
 # ----------------------------------------------------------------------------
