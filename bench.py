@@ -353,6 +353,8 @@ def run_gpu(args, rank, nranks, local, dist):
         ms_c, t_norm, t_fin, t_clip, launches_c, outcome = timed_clipped(args, grp, dplan, hp, stream, dist)
         norm_bytes = L.P * (2 * wl.world + 4)
         clip_bytes = L.P * 30
+        tr_norm = profiled_traffic("rs_direct_norm_bf16_w16" if wl.world == 16 else "rs_direct_norm")
+        tr_clip = profiled_traffic("adam_clip_w16" if wl.world == 16 else "adam_clip")
         clipped = {
             "ms_per_step": round(ms_c, 4), "params_per_s": round(nranks * L.T / (ms_c / 1e3)),
             "max_norm": args.max_norm, "launches_per_step": round(launches_c / args.steps),
@@ -360,11 +362,15 @@ def run_gpu(args, rank, nranks, local, dist):
             "rs_direct_norm": {"ms_per_step": round(t_norm / args.steps, 4),
                                "GB_per_s": round(gbs(norm_bytes, t_norm), 1),
                                "frac_of_peak": round(gbs(norm_bytes, t_norm) / peak, 4),
-                               "bytes_per_param": 2 * wl.world + 4},
+                               "bytes_per_param": 2 * wl.world + 4,
+                               "traffic_per_launch": tr_norm["dram_bytes_per_launch"] if tr_norm else None,
+                               "algorithmic_bytes_per_launch": round(norm_bytes / nbk)},
             "grad_check_finalize": {"ms_per_step": round(t_fin / args.steps, 4)},
             "adam_clip_step": {"ms_per_step": round(t_clip / args.steps, 4),
                                "GB_per_s": round(gbs(clip_bytes, t_clip), 1),
-                               "frac_of_peak": round(gbs(clip_bytes, t_clip) / peak, 4), "bytes_per_param": 30},
+                               "frac_of_peak": round(gbs(clip_bytes, t_clip) / peak, 4), "bytes_per_param": 30,
+                               "traffic_per_launch": tr_clip["dram_bytes_per_launch"] if tr_clip else None,
+                               "algorithmic_bytes_per_launch": clip_bytes},
         }
 
     e2e = None
