@@ -396,6 +396,139 @@ def run_gpu(args, rank, nranks, local, dist):
     return out
 
 
+def run_gpu_micro(args, rank, nranks, local, dist):
+    """A workload whose gradients come from several micro-steps (the Llama 1.1B
+    configuration: 4 bf16 micro-steps summed into an fp32 main_grad buffer per
+    rank, laid out flat in bucket order, then the fused step). One step is
+    the whole path: zr_grad_accumulate_first for micro-step 0, zr_grad_accumulate
+    for the middle ones, and per bucket zr_rs_adam_fused_acc, which adds the
+    last micro-step while it averages. The unfolded sequence (every micro-step
+    accumulated, then zr_rs_adam_fused on the fp32 buffer) is timed beside it."""
+    import torch
+    from zero_partition_aware_gb300 import workloads as W
+    from zero_partition_aware_gb300 import zr
+    from zero_partition_aware_gb300.engine import DPGroup
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    wl = W_lookup(args)
+    S_ = wl.micro_steps
+    grp = DPGroup(list(wl.numel), wl.world, wl.bucket, grad_dtype=torch.float32, device=device,
+                  allocate_buckets=False)
+    L = grp.layout
+    gen = W.generator(device, 0)
+    master = torch.randn(L.T, generator=gen, device=device).mul_(wl.master_std)
+    mb = []
+    for _ in range(wl.world):
+        row = []
+        for _ in range(S_):
+            g = torch.zeros(L.P, dtype=torch.bfloat16, device=device)
+            g[: L.T].copy_(W.draw_grad(wl, L.T, gen, device))
+            row.append(g)
+        mb.append(row)
+    m = W.draw_state(wl, L.T, gen, device)
+    v = W.draw_state(wl, L.T, gen, device)
+    grp.load_flat(master, m, v)
+    del master, m, v
+    main = [torch.zeros(L.P, dtype=torch.float32, device=device) for _ in range(wl.world)]
+    main_views = grp.main_grad_views(main)
+    last_views = grp.main_grad_views([row[-1] for row in mb])
+    hp = W.AdamW(step=wl.adam.step)
+    stream = torch.cuda.current_stream()
+    nbk = L.n_buckets
+    peak, peak_kind = measured_peaks()
+    W_ = max(args.warmup, 3)
+
+    def accumulate(upto):
+        for k in range(wl.world):
+            zr.zr_grad_accumulate_first(main[k], mb[k][0], stream=stream)
+        for s_ in range(1, upto):
+            for k in range(wl.world):
+                zr.zr_grad_accumulate(main[k], mb[k][s_], stream=stream)
+
+    def timed(acc_upto, tail):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        dist.barrier()
+        torch.cuda.synchronize()
+        n0 = zr.zr_launch_count()
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            accumulate(acc_upto)
+            ev[k][1].record(stream)
+            tail()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        launches = zr.zr_launch_count() - n0
+        dist.barrier()
+        t_acc = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps))
+        t_tail = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps))
+        ms = dist.max(ev[0][0].elapsed_time(ev[-1][2]) / args.steps)
+        return ms, t_acc, t_tail, launches
+
+    folded = lambda: grp.step_in_place_acc(main_views, last_views, hp, stream=stream)
+    unfolded = lambda: grp.step_in_place(main_views, hp, stream=stream)
+    for _ in range(W_):
+        accumulate(S_ - 1)
+        folded()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms, t_acc, t_fold, launches = timed(S_ - 1, folded)
+    clk = clocks.stop()
+    for _ in range(W_):
+        accumulate(S_)
+        unfolded()
+    torch.cuda.synchronize()
+    ms_u, t_acc_u, t_fused_u, launches_u = timed(S_, unfolded)
+
+    N = wl.world
+    gbs = lambda byts, t: byts * args.steps / (t / 1e3) / 1e9
+    acc_bytes = L.P * N * (6 + 10 * (S_ - 2))      # first micro-step: read 2, write 4; the others read 6, write 4
+    fold_bytes = L.P * (6 * N + 26)                 # N x (fp32 main + bf16 last) + p, m, v r/w + bf16 param
+    acc_bytes_u = L.P * N * (6 + 10 * (S_ - 1))
+    fused_bytes_u = L.P * (4 * N + 26)
+    acc_gbs, fold_gbs = gbs(acc_bytes, t_acc), gbs(fold_bytes, t_fold)
+    dominant = ("grad_accumulate", acc_gbs, acc_bytes) if t_acc >= t_fold else ("rs_adam_fused_acc", fold_gbs,
+                                                                                fold_bytes)
+    launches_acc = N * (S_ - 1)
+    roofline = {"bound": "hbm", "achieved": round(dominant[1], 1), "peak": peak, "unit": "GB/s",
+                "frac": round(dominant[1] / peak, 4), "traffic": None, "kernel": dominant[0],
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": round(dominant[2] / (launches_acc if dominant[0] == "grad_accumulate"
+                                                                     else nbk))}
+    out = {"metric": METRIC, "value": round(nranks * L.T / (ms / 1e3)), "unit": UNIT, "n_gpus": nranks,
+           "steps": args.steps, "warmup": W_, "ms_per_step": round(ms, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": wl.name, "params": L.T, "padded": L.P, "world": N,
+                      "reduce_bucket_size": wl.bucket, "buckets": nbk, "micro_steps": S_,
+                      "grad_dtype": "bf16 micro-steps into fp32 main_grad (flat, bucket order)",
+                      "step": "zr_grad_accumulate_first + zr_grad_accumulate for micro-steps 0..S-2, then per "
+                              "bucket zr_rs_adam_fused_acc (last micro-step folded into the fused step)",
+                      "l2": "no flush: every launch's working set exceeds the 129 MB L2",
+                      "parallelism": f"replicas only x{nranks}"},
+           "roofline": roofline,
+           "kernels": {
+               "grad_accumulate": {"ms_per_step": round(t_acc / args.steps, 4), "GB_per_s": round(acc_gbs, 1),
+                                   "frac_of_peak": round(acc_gbs / peak, 4),
+                                   "bytes_per_param": N * (6 + 10 * (S_ - 2)), "launches_per_step": launches_acc},
+               "rs_adam_fused_acc": {"ms_per_step": round(t_fold / args.steps, 4), "GB_per_s": round(fold_gbs, 1),
+                                     "frac_of_peak": round(fold_gbs / peak, 4), "bytes_per_param": 6 * N + 26,
+                                     "launches_per_step": nbk}},
+           "unfolded_step": {
+               "ms_per_step": round(ms_u, 4), "params_per_s": round(nranks * L.T / (ms_u / 1e3)),
+               "grad_accumulate": {"ms_per_step": round(t_acc_u / args.steps, 4),
+                                   "GB_per_s": round(gbs(acc_bytes_u, t_acc_u), 1),
+                                   "bytes_per_param": N * (6 + 10 * (S_ - 1))},
+               "rs_adam_fused": {"ms_per_step": round(t_fused_u / args.steps, 4),
+                                 "GB_per_s": round(gbs(fused_bytes_u, t_fused_u), 1),
+                                 "frac_of_peak": round(gbs(fused_bytes_u, t_fused_u) / peak, 4),
+                                 "bytes_per_param": 4 * N + 26}},
+           "gpu_launches": int(launches), "clocks": clk,
+           "e2e": None, "e2e_note": "not run for micro-step workloads: 4 micro-steps of bf16 grads are 70 GB"}
+    return out
+
+
 def run_e2e(args, wl, grp, arenas, dplan, hp, stream, nranks, dist):
     """The same step through the public API with the gradients starting in pinned
     host memory: per step, H2D of every rank's gradients, the step, D2H of the
@@ -466,16 +599,27 @@ def oracle_sample(wl, n_elems, seed=0):
     sub = W.replace(wl, numel=tuple(numel))
     lay = oracle.layout(numel, wl.world, wl.bucket)
     inp = W.draw_inputs(sub, "cpu", seed=seed)
-    grads = [oracle.params_from_flat(lay, W.bf16_bits(inp["grads"][k][0])) for k in range(wl.world)]
+    if wl.micro_steps > 1:  # the micro-steps' flat bf16 grads, accumulated inside the timed step
+        grads = [[W.bf16_bits(g) for g in inp["grads"][k]] for k in range(wl.world)]
+    else:
+        grads = [oracle.params_from_flat(lay, W.bf16_bits(inp["grads"][k][0])) for k in range(wl.world)]
     p = oracle.shards_from_flat(lay, inp["master"].numpy())
     m = oracle.shards_from_flat(lay, inp["m"].numpy())
     v = oracle.shards_from_flat(lay, inp["v"].numpy())
     return lay, grads, p, m, v
 
 
-def oracle_step(lay, grads, p, m, v, hp, scale):
+def oracle_step(lay, grads, p, m, v, hp, scale, micro=False):
     import oracle
     param = np.zeros(lay.P, np.uint16)
+    if micro:  # every micro-step into an fp32 main_grad per rank, then its buckets
+        mains = []
+        for row in grads:
+            acc = np.zeros(lay.T, np.float32)
+            for g in row:
+                oracle.grad_accumulate(acc, g)
+            mains.append(oracle.params_from_flat(lay, acc))
+        grads = mains
     for b in range(lay.n_buckets):
         bucket = oracle.bucket_pack(lay, b, grads)
         oracle.rs_adam_fused(lay, b, bucket, scale, p, m, v, hp, param)
@@ -493,12 +637,13 @@ def cpu_baseline(wl, budget_s):
     reps, dt = 0, 0.0
     while dt < budget_s and reps < 1000:
         t0 = time.perf_counter()
-        oracle_step(lay, grads, p, m, v, wl.adam, scale)
+        oracle_step(lay, grads, p, m, v, wl.adam, scale, micro=wl.micro_steps > 1)
         dt += time.perf_counter() - t0
         reps += 1
     return {"value": round(reps * lay.T / dt), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {lay.n_params} params ({lay.T} elements) of {wl.name}, world {wl.world}: "
-                      f"pack + fused step run {reps} times, {dt:.1f} s single-threaded",
+                      + (f"{wl.micro_steps} micro-step accumulations + " if wl.micro_steps > 1 else "")
+                      + f"pack + fused step run {reps} times, {dt:.1f} s single-threaded",
             "seconds": round(dt, 2)}
 
 
@@ -511,19 +656,20 @@ def run_reference(args):
     # each step: a bounded sample (~2 s of single-threaded oracle work)
     lay, grads, p, m, v = oracle_sample(wl, 200_000)
     t0 = time.perf_counter()
-    oracle_step(lay, grads, p, m, v, wl.adam, scale)
+    oracle_step(lay, grads, p, m, v, wl.adam, scale, micro=wl.micro_steps > 1)
     rate = lay.T / max(time.perf_counter() - t0, 1e-6)
     per_step = max(2.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
     lay, grads, p, m, v = oracle_sample(wl, int(min(max(rate * per_step, 200_000), 1 << 24)))
     for _ in range(args.warmup):
-        oracle_step(lay, grads, p, m, v, wl.adam, scale)
+        oracle_step(lay, grads, p, m, v, wl.adam, scale, micro=wl.micro_steps > 1)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(lay, grads, p, m, v, wl.adam, scale)
+        oracle_step(lay, grads, p, m, v, wl.adam, scale, micro=wl.micro_steps > 1)
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     value = lay.T / dt
     sample = (f"first {lay.n_params} params ({lay.T} elements) of {wl.name}, world {wl.world}: "
-              f"pack + fused step per timed step")
+              + (f"{wl.micro_steps} micro-step accumulations + " if wl.micro_steps > 1 else "")
+              + "pack + fused step per timed step")
     return {"impl": "reference", "metric": METRIC, "value": round(value), "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -546,7 +692,7 @@ def main():
     if rank == 0:
         build.build()
     dist.barrier()
-    out = run_gpu(args, rank, nranks, local, dist)
+    out = (run_gpu_micro if W_lookup(args).micro_steps > 1 else run_gpu)(args, rank, nranks, local, dist)
     if rank == 0:
         if nranks == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(W_lookup(args), args.cpu_seconds)

@@ -248,6 +248,14 @@ int zr_grad_accumulate(float *main_grad, const void *g, zr_dtype g_dtype, int64_
                        zr_stream stream);
 
 /*
+ * The first micro-step of an accumulation: main_grad[e] = 0 + float(g[e]),
+ * the value zr_grad_accumulate gives on a zeroed buffer (0 + -0 is +0),
+ * without reading main_grad or zeroing it first.
+ */
+int zr_grad_accumulate_first(float *main_grad, const void *g, zr_dtype g_dtype, int64_t n,
+                             zr_stream stream);
+
+/*
  * Reduce-scatter with average over one bucket ([DS] §三.2 and §六: predivide
  * by the data-parallel size, then reduce each slice to its owner; [IQ]
  * §"三种原语": GPU i gets segment i of the sum; [DS] §三.3
@@ -306,6 +314,28 @@ int zr_rs_adam_fused(const zr_layout *layout, int64_t bucket, const void *const 
                      zr_dtype dtype, float scale, float *const *master, float *const *m,
                      float *const *v, const zr_adamw *hp, void *param_bf16,
                      float *const *shard_grad_out, zr_stream stream);
+
+/*
+ * zr_rs_adam_fused with the last micro-step's accumulation folded in ([MG]
+ * §"四步接力": every micro-step's 16-bit grad is added into the fp32 main_grad
+ * before the bucket is reduced; §"通信模式"): for bucket position e,
+ *   g_k[e] = fp32(main_in[k][e] + last_in[k][e]),
+ * then the averaging, AdamW and cast of zr_rs_adam_fused over the g_k. The
+ * results equal zr_grad_accumulate of last_in[k] into main_in[k] followed by
+ * zr_rs_adam_fused on main_in, bit for bit, but main_in is only read: the
+ * accumulated main_grad is never stored, which saves writing it and reading
+ * it back (8 of the 14 bytes per replica and element of the unfused pair).
+ * main_in: host array [world] of device pointers, numel_b fp32 each (the
+ *   contiguous main_grad buffer's bucket, holding the earlier micro-steps).
+ * last_in: host array [world] of device pointers, numel_b elements of
+ *   last_dtype (ZR_BF16 or ZR_FP16) each, in the same bucket order.
+ * world <= 32 (ZR_ERR_UNSUPPORTED above). Other arguments as for
+ * zr_rs_adam_fused.
+ */
+int zr_rs_adam_fused_acc(const zr_layout *layout, int64_t bucket, const float *const *main_in,
+                         const void *const *last_in, zr_dtype last_dtype, float scale, float *const *master,
+                         float *const *m, float *const *v, const zr_adamw *hp, void *param_bf16,
+                         float *const *shard_grad_out, zr_stream stream);
 
 /*
  * Steps 1 to 4 in one pass, without a bucket buffer. A direct plan records,

@@ -209,7 +209,8 @@ class DPGroup:
         return list(zip(lo, hi))
 
     def main_grad_views(self, main_grad: Sequence[torch.Tensor]) -> List[zr.PtrArray]:
-        """Per-bucket pointer arrays into flat [P] fp32 per-rank grad buffers: the
+        """Per-bucket pointer arrays into flat [P] per-rank grad buffers (fp32
+        main_grad, or a micro-step's 16-bit grads laid out the same way): the
         Megatron-style contiguous buffer is already bucket-ordered, so its
         buckets are read in place without packing."""
         es = main_grad[0].element_size()
@@ -222,3 +223,14 @@ class DPGroup:
     def step_in_place(self, bucket_views: Sequence[zr.PtrArray], hp, stream=None) -> None:
         for b in range(self.layout.n_buckets):
             self.fused(b, hp, bucket_in=bucket_views[b], stream=stream)
+
+    def step_in_place_acc(self, main_views: Sequence[zr.PtrArray], last_views: Sequence[zr.PtrArray], hp,
+                          last_dtype=zr.ZR_BF16, stream=None) -> None:
+        """The step with the last micro-step folded in: for every bucket, the
+        fp32 main_grad (the earlier micro-steps) plus the last micro-step's
+        16-bit grads are averaged, and AdamW + cast run, in one pass; the
+        accumulated main_grad is never written ("Megatron-LM 分布式训练（四）"
+        §"四步接力": micro-step grads are summed into main_grad, then reduced)."""
+        for b in range(self.layout.n_buckets):
+            zr.zr_rs_adam_fused_acc(self.layout, b, main_views[b], last_views[b], self.scale, self._p_master,
+                                    self._p_m, self._p_v, hp, self.param, last_dtype=last_dtype, stream=stream)

@@ -100,11 +100,14 @@ _SIGS = {
     "zr_bucket_pack_planned": (ctypes.c_int, [_vp, _i64, _vp]),
     "zr_bucket_pack_noalloc": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
     "zr_grad_accumulate": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
+    "zr_grad_accumulate_first": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_reduce_scatter_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
     "zr_adam_shard_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _P(zr_adamw), _vp]),
     "zr_gather_cast_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "zr_rs_adam_fused": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp, _vp,
                                         _P(zr_adamw), _vp, _vp, _vp]),
+    "zr_rs_adam_fused_acc": (ctypes.c_int, [_vp, _i64, _vp, _vp, ctypes.c_int, _f32, _vp, _vp, _vp,
+                                            _P(zr_adamw), _vp, _vp, _vp]),
     "zr_allreduce_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _f32, _vp, _vp]),
     "zr_direct_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _P(_vp)]),
     "zr_direct_plan_destroy": (ctypes.c_int, [_vp]),
@@ -407,6 +410,16 @@ def zr_grad_accumulate(main_grad, g, n: Optional[int] = None, dtype=None, stream
     _check(_lib.zr_grad_accumulate(_addr(main_grad), _addr(g), d, int(n), _stream(stream)), "zr_grad_accumulate")
 
 
+def zr_grad_accumulate_first(main_grad, g, n: Optional[int] = None, dtype=None, stream=None) -> None:
+    if n is None:
+        n = int(main_grad.numel())
+        if int(g.numel()) != n:
+            raise ValueError("main_grad and g sizes differ")
+    d = _dtype_of([g], dtype)
+    _check(_lib.zr_grad_accumulate_first(_addr(main_grad), _addr(g), d, int(n), _stream(stream)),
+           "zr_grad_accumulate_first")
+
+
 def zr_reduce_scatter_avg(layout: Layout, bucket: int, bucket_in, scale: float, shard_grad,
                           dtype=None, stream=None) -> None:
     d = _dtype_of(bucket_in, dtype)
@@ -437,6 +450,16 @@ def zr_rs_adam_fused(layout: Layout, bucket: int, bucket_in, scale: float, maste
     _check(_lib.zr_rs_adam_fused(layout.handle, int(bucket), px.ptr, d, float(scale), pm.ptr, pmm.ptr, pv.ptr,
                                  ctypes.byref(h), _addr(param_bf16), go.ptr if go is not None else None,
                                  _stream(stream)), "zr_rs_adam_fused")
+
+
+def zr_rs_adam_fused_acc(layout: Layout, bucket: int, main_in, last_in, scale: float, master, m, v, hp,
+                         param_bf16=None, shard_grad_out=None, last_dtype=None, stream=None) -> None:
+    d = _dtype_of(last_in, last_dtype)
+    h = _hp(hp)
+    px, py, pm, pmm, pv, go = _ptrs(main_in), _ptrs(last_in), _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(shard_grad_out)
+    _check(_lib.zr_rs_adam_fused_acc(layout.handle, int(bucket), px.ptr, py.ptr, d, float(scale), pm.ptr, pmm.ptr,
+                                     pv.ptr, ctypes.byref(h), _addr(param_bf16), go.ptr if go is not None else None,
+                                     _stream(stream)), "zr_rs_adam_fused_acc")
 
 
 class DirectPlan:
