@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--impl", default="zr", choices=["zr", "reference"])
     ap.add_argument("--workload", default="irregular_10k")
     ap.add_argument("--world", type=int, default=0, help="override the workload's emulated replica count")
+    ap.add_argument("--bucket", type=int, default=0, help="override the workload's reduce_bucket_size")
     ap.add_argument("--arrival", default="flat", choices=["flat", "reverse"],
                     help="gradient arrival order that fills the buckets (reverse: backward's order)")
     ap.add_argument("--max-norm", type=float, default=1.0,
@@ -261,8 +262,7 @@ def timed_clipped(args, grp, dplan, hp, stream, dist):
     start_ev.record(stream)
     for k in range(args.steps):
         ev[k][0].record(stream)
-        for b in range(nbk):
-            zr.zr_rs_direct_norm(dplan, b, grp.scale, grp._p_grad, grp.check, stream=stream)
+        zr.zr_rs_direct_norm_range(dplan, 0, nbk, grp.scale, grp._p_grad, grp.check, stream=stream)
         ev[k][1].record(stream)
         zr.zr_grad_check_finalize(grp.check, args.max_norm, stream=stream)
         ev[k][2].record(stream)
@@ -297,19 +297,27 @@ def run_gpu(args, rank, nranks, local, dist):
     W_ = max(args.warmup, 3)
 
     direct = lambda b: grp.direct(b, dplan, hp, stream=stream)
+    direct_all = lambda _: grp.step_direct(dplan, hp, stream=stream)
     pack = lambda b: grp.pack_planned(b, plan, stream)
     fused = lambda b: grp.fused(b, hp, stream=stream)
 
-    # the headline step: steps 1-4 in one pass per bucket (no bucket buffer)
+    # the headline step: steps 1-4 in one pass for every bucket (no bucket buffer), consecutive
+    # buckets sharing launches (zr_step_direct_range)
     for _ in range(W_):
-        for b in range(nbk):
-            direct(b)
+        direct_all(0)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    ms_step, t_direct, _, launches = timed_steps(args, nbk, direct, None, stream, dist)
+    ms_step, t_direct, _, launches = timed_steps(args, 1, direct_all, None, stream, dist)
     clk = clocks.stop()
+
+    # the same step with one launch per bucket (zr_step_direct), as buckets reduced while backward fills them
+    for _ in range(W_):
+        for b in range(nbk):
+            direct(b)
+    torch.cuda.synchronize()
+    ms_pb, t_pb, _, launches_pb = timed_steps(args, nbk, direct, None, stream, dist)
 
     # the same step with the bucket materialised: planned pack, then the fused kernel
     for _ in range(W_):
@@ -319,20 +327,44 @@ def run_gpu(args, rank, nranks, local, dist):
     torch.cuda.synchronize()
     ms_two, t_pack, t_fused, launches_two = timed_steps(args, nbk, pack, fused, stream, dist)
 
+    # the same two kernels with packing overlapped: bucket b+1 packed on a second stream while b is reduced
+    plans2 = grp.overlap_plans(table)
+    side = torch.cuda.Stream()
+    for _ in range(W_):
+        grp.step_overlapped(plans2, hp, stream=stream, side_stream=side)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        grp.step_overlapped(plans2, hp, stream=stream, side_stream=side)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms_ov = dist.max(ev0.elapsed_time(ev1) / args.steps)
+
     value = nranks * L.T / (ms_step / 1e3)
     gbs = lambda byts, ms: byts * args.steps / (ms / 1e3) / 1e9
     direct_gbs, pack_gbs, fused_gbs = gbs(fused_bytes, t_direct), gbs(pack_bytes, t_pack), gbs(fused_bytes, t_fused)
+    launches_per_step = max(1, round(launches / args.steps))
     kname = "rs_direct_bf16_w16" if wl.world == 16 else "rs_direct"
     tr = profiled_traffic(kname)
+    elems_per_launch = L.P / launches_per_step
     roofline = {"bound": "hbm", "achieved": round(direct_gbs, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(direct_gbs / peak, 4), "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "frac": round(direct_gbs / peak, 4),
+                "traffic": round(tr["dram_bytes_per_element"] * elems_per_launch) if tr else None,
                 "kernel": kname, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "algorithmic_bytes_per_launch": round(fused_bytes / nbk)}
+                "algorithmic_bytes_per_launch": round(fused_bytes / launches_per_step)}
+    pb_gbs = gbs(fused_bytes, t_pb)
     kernels = {
         "rs_direct": {"ms_per_step": round(t_direct / args.steps, 4), "GB_per_s": round(direct_gbs, 1),
                       "frac_of_peak": round(direct_gbs / peak, 4), "bytes_per_param": 2 * wl.world + 26,
-                      "launches_per_step": nbk},
+                      "launches_per_step": launches_per_step},
+        "rs_direct_per_bucket": {"ms_per_step": round(ms_pb, 4), "params_per_s": round(nranks * L.T / (ms_pb / 1e3)),
+                                 "GB_per_s": round(pb_gbs, 1), "frac_of_peak": round(pb_gbs / peak, 4),
+                                 "launches_per_step": round(launches_pb / args.steps)},
     }
     two_kernel = {
         "ms_per_step": round(ms_two, 4), "params_per_s": round(nranks * L.T / (ms_two / 1e3)),
@@ -341,6 +373,10 @@ def run_gpu(args, rank, nranks, local, dist):
                         "frac_of_peak": round(pack_gbs / peak, 4), "bytes_per_param": 4 * wl.world},
         "rs_adam_fused": {"ms_per_step": round(t_fused / args.steps, 4), "GB_per_s": round(fused_gbs, 1),
                           "frac_of_peak": round(fused_gbs / peak, 4), "bytes_per_param": 2 * wl.world + 26},
+        "overlapped": {"ms_per_step": round(ms_ov, 4), "params_per_s": round(nranks * L.T / (ms_ov / 1e3)),
+                       "GB_per_s": round(gbs(pack_bytes + fused_bytes, ms_ov * args.steps), 1),
+                       "how": "pack of bucket b+1 on a second stream while bucket b is reduced; two bucket "
+                              "buffer sets, ordered by events"},
     }
 
     clipped = None
@@ -363,14 +399,12 @@ def run_gpu(args, rank, nranks, local, dist):
                                "GB_per_s": round(gbs(norm_bytes, t_norm), 1),
                                "frac_of_peak": round(gbs(norm_bytes, t_norm) / peak, 4),
                                "bytes_per_param": 2 * wl.world + 4,
-                               "traffic_per_launch": tr_norm["dram_bytes_per_launch"] if tr_norm else None,
-                               "algorithmic_bytes_per_launch": round(norm_bytes / nbk)},
+                               "traffic_per_element": tr_norm["dram_bytes_per_element"] if tr_norm else None},
             "grad_check_finalize": {"ms_per_step": round(t_fin / args.steps, 4)},
             "adam_clip_step": {"ms_per_step": round(t_clip / args.steps, 4),
                                "GB_per_s": round(gbs(clip_bytes, t_clip), 1),
                                "frac_of_peak": round(gbs(clip_bytes, t_clip) / peak, 4), "bytes_per_param": 30,
-                               "traffic_per_launch": tr_clip["dram_bytes_per_launch"] if tr_clip else None,
-                               "algorithmic_bytes_per_launch": clip_bytes},
+                               "traffic_per_element": tr_clip["dram_bytes_per_element"] if tr_clip else None},
         }
 
     e2e = None
@@ -384,7 +418,8 @@ def run_gpu(args, rank, nranks, local, dist):
                       "reduce_bucket_size": wl.bucket, "buckets": nbk, "grad_dtype": "bf16",
                       "grad_layout": "per-parameter tensors, 512-byte aligned starts",
                       "arrival": args.arrival,
-                      "step": "per bucket: zr_step_direct (pack + reduce-scatter + AdamW + bf16 cast in one pass)",
+                      "step": "zr_step_direct_range over every bucket (pack + reduce-scatter + AdamW + bf16 cast in "
+                              "one pass; consecutive buckets share launches)",
                       "l2": "no flush: every bucket's working set (~1 GB) exceeds the 129 MB L2",
                       "parallelism": f"replicas only x{nranks}"},
            "roofline": roofline, "kernels": kernels, "two_kernel_step": two_kernel,
@@ -705,7 +740,11 @@ def W_lookup(args):
     """The workload named by --workload, with --world applied."""
     from zero_partition_aware_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
-    return W.replace(wl, world=args.world) if args.world else wl
+    if args.world:
+        wl = W.replace(wl, world=args.world)
+    if args.bucket:
+        wl = W.replace(wl, bucket=args.bucket)
+    return wl
 
 
 if __name__ == "__main__":

@@ -364,6 +364,21 @@ int zr_step_direct(const zr_direct_plan *plan, int64_t bucket, float scale, floa
                    float *const *shard_grad_out, zr_stream stream);
 
 /*
+ * zr_step_direct for buckets [bucket_first, bucket_first + bucket_count), in
+ * as few launches as the launch parameters allow (consecutive buckets share
+ * one while their runs, their tables and their boundary tiles fit: 256 runs,
+ * 16 buckets and 1,024 listed tiles). The buckets' elements are disjoint, so
+ * the results equal bucket_count calls of zr_step_direct bit for bit; longer
+ * launches spend less of their time filling and draining the pipelines. For
+ * a step that runs once every bucket's gradients are ready (after backward,
+ * or at a gradient-accumulation boundary); a step that reduces buckets as
+ * backward fills them calls zr_step_direct per bucket.
+ */
+int zr_step_direct_range(const zr_direct_plan *plan, int64_t bucket_first, int64_t bucket_count, float scale,
+                         float *const *master, float *const *m, float *const *v, const zr_adamw *hp,
+                         void *param_bf16, float *const *shard_grad_out, zr_stream stream);
+
+/*
  * All-reduce with average over one bucket, the path used when
  * reduce_scatter is off ([DS] §三.2 gradient_reduction_w_predivide; [MG]
  * §"四步接力" step 4; [IQ] §"三种原语"): out[k][e] = the same averaged value
@@ -445,6 +460,11 @@ int zr_reduce_scatter_avg_norm(const zr_layout *layout, int64_t bucket, const vo
  */
 int zr_rs_direct_norm(const zr_direct_plan *plan, int64_t bucket, float scale, float *const *shard_grad,
                       zr_gradcheck *chk, zr_stream stream);
+
+/* zr_rs_direct_norm for buckets [bucket_first, bucket_first + bucket_count),
+ * grouped into launches as zr_step_direct_range groups them. */
+int zr_rs_direct_norm_range(const zr_direct_plan *plan, int64_t bucket_first, int64_t bucket_count, float scale,
+                            float *const *shard_grad, zr_gradcheck *chk, zr_stream stream);
 
 /*
  * Once every bucket has been added: sums chk's accumulators in a fixed

@@ -72,3 +72,35 @@ def test_from_host_equals_device_resident(mods, world, n, hi, B):
     for r in range(world):
         for a, b in ((got.master[r], ref.master[r]), (got.m[r], ref.m[r]), (got.v[r], ref.v[r])):
             assert np.array_equal(_bits(a), _bits(b)), r
+
+
+@pytest.mark.parametrize("world,n,hi,B", [(4, 40, 30_000, 60_000), (16, 120, 200_000, 1 << 21), (8, 5, 1000, 1)])
+def test_overlapped_pack_and_fused_equal_the_sequential_step(mods, world, n, hi, B):
+    """Packing bucket b+1 on a second stream while bucket b is reduced (two
+    bucket buffer sets) gives the sequential step's results bit for bit."""
+    engine, zr = mods
+    rng = np.random.default_rng(100 + world)
+    numel = W.random_numels(rng, n, 1, hi)
+    wl = W.Workload("ov", tuple(numel), world, B, ("normal", 1e-2), 0.02, ("absnormal", 1e-4), W.AdamW(step=2))
+    inp = W.draw_inputs(wl, "cuda", seed=world)
+    hp = W.AdamW(step=2)
+    groups = []
+    for _ in range(2):
+        g = engine.DPGroup(numel, world, B, device="cuda")
+        g.load_flat(inp["master"], inp["m"], inp["v"])
+        groups.append(g)
+    L = groups[0].layout
+    rows = [[inp["grads"][k][0][L.param(i)[0]: L.param(i)[0] + numel[i]] for i in range(len(numel))]
+            for k in range(world)]
+    a, b = groups
+    ta, tb = a.grad_table(rows), b.grad_table(rows)
+    a.step(ta, hp, plan=a.pack_plan(ta))
+    plans = b.overlap_plans(tb)
+    for _ in range(2):  # twice: the second step reuses both buffer sets
+        b.step_overlapped(plans, hp)
+    a.step(ta, hp, plan=a.pack_plan(ta))
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(a.param[: L.P]), _bits(b.param[: L.P]))
+    for r in range(world):
+        for x, y in ((a.master[r], b.master[r]), (a.m[r], b.m[r]), (a.v[r], b.v[r])):
+            assert np.array_equal(_bits(x), _bits(y)), r

@@ -93,6 +93,49 @@ class DPGroup:
                 self.pack(b, grad_table, stream)
             self.fused(b, hp, stream=stream)
 
+    def overlap_plans(self, grad_table: zr.PtrArray):
+        """Two pack plans over two sets of bucket buffers, for step_overlapped:
+        bucket b+1 is packed into one set while bucket b is reduced from the
+        other (allocated on first use)."""
+        if not getattr(self, "_buckets2", None):
+            self._buckets2 = [torch.empty(max(self.max_bucket, 1), dtype=self.grad_dtype, device=self.device)
+                              for _ in range(self.world)]
+            self._p_buckets2 = zr.PtrArray(self._buckets2)
+        return (zr.PackPlan(self.layout, grad_table, self._p_buckets, dtype=self.zr_dtype),
+                zr.PackPlan(self.layout, grad_table, self._p_buckets2, dtype=self.zr_dtype))
+
+    def step_overlapped(self, plans, hp, stream=None, side_stream=None) -> None:
+        """The two-kernel step with packing and reduction overlapped
+        ("DeepSpeed ZeRO 通信优化深度解析" §四, §五 overlap_comm: the copy into the
+        IPG bucket and the reduction of the previous bucket run on different
+        streams): bucket b+1 is packed on side_stream into one buffer set while
+        the fused step reduces bucket b from the other. Events order each
+        buffer's reuse; nothing waits on the device. `stream` waits for all
+        of it at the end."""
+        cur = stream or torch.cuda.current_stream(self.device)
+        side = side_stream or torch.cuda.Stream(self.device)
+        nb = self.layout.n_buckets
+        if nb == 0:
+            return
+        sets = (self._p_buckets, self._p_buckets2)
+        packed = [torch.cuda.Event() for _ in range(nb)]
+        used = [torch.cuda.Event() for _ in range(nb)]
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            zr.zr_bucket_pack_planned(plans[0], 0, stream=side)
+            packed[0].record(side)
+        for b in range(nb):
+            if b + 1 < nb:
+                with torch.cuda.stream(side):
+                    if b >= 1:
+                        side.wait_event(used[b - 1])  # buffer set (b+1) % 2 was read by bucket b-1
+                    zr.zr_bucket_pack_planned(plans[(b + 1) % 2], b + 1, stream=side)
+                    packed[b + 1].record(side)
+            cur.wait_event(packed[b])
+            self.fused(b, hp, bucket_in=sets[b % 2], stream=cur)
+            used[b].record(cur)
+        cur.wait_stream(side)
+
     def direct_plan(self, grad_table: zr.PtrArray) -> zr.DirectPlan:
         """Device-resident map of these gradient tensors for the direct step (build once)."""
         return zr.DirectPlan(self.layout, grad_table, dtype=self.zr_dtype)
@@ -102,10 +145,17 @@ class DPGroup:
         zr.zr_step_direct(plan, b, self.scale, self._p_master, self._p_m, self._p_v, hp,
                           self.param if write_param else None, shard_grad_out, stream=stream)
 
-    def step_direct(self, plan: zr.DirectPlan, hp, stream=None) -> None:
-        """Every bucket in order, steps 1-4 in one pass each, no bucket buffer."""
-        for b in range(self.layout.n_buckets):
-            self.direct(b, plan, hp, stream=stream)
+    def step_direct(self, plan: zr.DirectPlan, hp, stream=None, per_bucket: bool = False) -> None:
+        """Steps 1-4 for every bucket in one pass each, no bucket buffer: one
+        zr_step_direct_range call, which groups consecutive buckets into as few
+        launches as it can (per_bucket: one zr_step_direct call per bucket, as a
+        step that reduces buckets while backward fills them runs)."""
+        if per_bucket:
+            for b in range(self.layout.n_buckets):
+                self.direct(b, plan, hp, stream=stream)
+            return
+        zr.zr_step_direct_range(plan, 0, self.layout.n_buckets, self.scale, self._p_master, self._p_m, self._p_v,
+                                hp, self.param, stream=stream)
 
     # ---- the step with a global gradient check ---------------------------------------
     def grad_shards(self) -> List[torch.Tensor]:
@@ -129,8 +179,7 @@ class DPGroup:
         the check found an overflow. The outcome stays on the device
         (``zr.zr_gradcheck_read(self.check)`` reads it)."""
         self.grad_shards()
-        for b in range(self.layout.n_buckets):
-            zr.zr_rs_direct_norm(plan, b, self.scale, self._p_grad, self.check, stream=stream)
+        zr.zr_rs_direct_norm_range(plan, 0, self.layout.n_buckets, self.scale, self._p_grad, self.check, stream=stream)
         self.finish_clipped(hp, max_norm, stream)
 
     def step_clipped(self, grad_table: zr.PtrArray, hp, max_norm: float, stream=None,

@@ -112,6 +112,8 @@ _SIGS = {
     "zr_direct_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _P(_vp)]),
     "zr_direct_plan_destroy": (ctypes.c_int, [_vp]),
     "zr_step_direct": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
+    "zr_step_direct_range": (ctypes.c_int, [_vp, _i64, _i64, _f32, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
+    "zr_rs_direct_norm_range": (ctypes.c_int, [_vp, _i64, _i64, _f32, _vp, _vp, _vp]),
     "zr_gradcheck_create": (ctypes.c_int, [_P(_vp)]),
     "zr_gradcheck_destroy": (ctypes.c_int, [_vp]),
     "zr_gradcheck_reset": (ctypes.c_int, [_vp, _vp]),
@@ -510,6 +512,15 @@ def zr_step_direct(plan: DirectPlan, bucket: int, scale: float, master, m, v, hp
            "zr_step_direct")
 
 
+def zr_step_direct_range(plan: DirectPlan, bucket_first: int, bucket_count: int, scale: float, master, m, v, hp,
+                         param_bf16=None, shard_grad_out=None, stream=None) -> None:
+    h = _hp(hp)
+    pm, pmm, pv, go = _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(shard_grad_out)
+    _check(_lib.zr_step_direct_range(plan.handle, int(bucket_first), int(bucket_count), float(scale), pm.ptr,
+                                     pmm.ptr, pv.ptr, ctypes.byref(h), _addr(param_bf16),
+                                     go.ptr if go is not None else None, _stream(stream)), "zr_step_direct_range")
+
+
 def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, dtype=None, stream=None,
                      postscale: float = 1.0) -> None:
     d = _dtype_of(bucket_in, dtype)
@@ -568,6 +579,13 @@ def zr_rs_direct_norm(plan: DirectPlan, bucket: int, scale: float, shard_grad, c
     g = _ptrs(shard_grad)
     _check(_lib.zr_rs_direct_norm(plan.handle, int(bucket), float(scale), g.ptr, chk.handle, _stream(stream)),
            "zr_rs_direct_norm")
+
+
+def zr_rs_direct_norm_range(plan: DirectPlan, bucket_first: int, bucket_count: int, scale: float, shard_grad,
+                            chk: GradCheck, stream=None) -> None:
+    g = _ptrs(shard_grad)
+    _check(_lib.zr_rs_direct_norm_range(plan.handle, int(bucket_first), int(bucket_count), float(scale), g.ptr,
+                                        chk.handle, _stream(stream)), "zr_rs_direct_norm_range")
 
 
 def zr_grad_check_finalize(chk: GradCheck, max_norm: float, stream=None) -> None:
