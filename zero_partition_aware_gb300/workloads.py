@@ -119,6 +119,14 @@ WORKLOADS["irregular_prof"] = Workload(
     description="first 400 params of irregular_10k, world=16, bucket 2^24 (profiling size)")
 
 
+# The Llama 1.1B micro-step path at profiling size: the first decoder layer's
+# nine tensors (44.0 M elements, one bucket), world 8, 4 bf16 micro-steps.
+WORKLOADS["llama_prof"] = Workload(
+    "llama_prof", WORKLOADS["llama_1p1b"].numel[1:10], 8, 500_000_000,
+    ("normal", 1e-3), 0.02, ("absnormal", 1e-4), _STEP10, micro_steps=4,
+    description="first decoder layer of llama_1p1b, world=8, 4 micro-steps (profiling size)")
+
+
 def replace(wl: Workload, **kw) -> Workload:
     return dataclasses.replace(wl, **kw)
 
