@@ -530,8 +530,13 @@ def run_gpu_micro(args, rank, nranks, local, dist):
     dominant = ("grad_accumulate", acc_gbs, acc_bytes) if t_acc >= t_fold else ("rs_adam_fused_acc", fold_gbs,
                                                                                 fold_bytes)
     launches_acc = N * (S_ - 1)
+    is_acc = dominant[0] == "grad_accumulate"
+    tr = profiled_traffic("grad_accumulate_bf16" if is_acc else ("rs_adam_fused_acc_w8" if N == 8 else "none"))
+    elems_per_launch = L.P if is_acc else L.P / nbk
     roofline = {"bound": "hbm", "achieved": round(dominant[1], 1), "peak": peak, "unit": "GB/s",
-                "frac": round(dominant[1] / peak, 4), "traffic": None, "kernel": dominant[0],
+                "frac": round(dominant[1] / peak, 4),
+                "traffic": round(tr["dram_bytes_per_element"] * elems_per_launch) if tr else None,
+                "kernel": dominant[0],
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": round(dominant[2] / (launches_acc if dominant[0] == "grad_accumulate"
