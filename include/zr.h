@@ -365,9 +365,10 @@ int zr_step_direct(const zr_direct_plan *plan, int64_t bucket, float scale, floa
 
 /*
  * zr_step_direct for buckets [bucket_first, bucket_first + bucket_count), in
- * as few launches as the launch parameters allow (consecutive buckets share
- * one while their runs, their tables and their boundary tiles fit: 256 runs,
- * 16 buckets and 1,024 listed tiles). The buckets' elements are disjoint, so
+ * few launches: consecutive buckets share one while their runs, their tables
+ * and their boundary tiles fit the launch parameters (256 runs, 16 buckets and
+ * 1,024 listed tiles) and the launch stays within 2^26 elements; a longer run
+ * gets a launch of its own. The buckets' elements are disjoint, so
  * the results equal bucket_count calls of zr_step_direct bit for bit; longer
  * launches spend less of their time filling and draining the pipelines. For
  * a step that runs once every bucket's gradients are ready (after backward,
