@@ -241,3 +241,36 @@ def test_gradient_check_create_without_device_reports_state(zr):
     h = ctypes.c_void_p()
     assert zr._lib.zr_gradcheck_create(ctypes.byref(h)) in (zr.ZR_ERR_STATE, zr.ZR_ERR_OOM, zr.ZR_ERR_CUDA)
     assert not h.value
+
+
+def test_range_folded_and_first_validate_before_launch(zr):
+    """zr_step_direct_range, zr_rs_direct_norm_range, zr_rs_adam_fused_acc and
+    zr_grad_accumulate_first reject bad arguments on the host."""
+    lay = zr.Layout([100, 200], 2, 1000)
+    L = zr._lib
+    two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    odd = (ctypes.c_void_p * 2)(0x1002, 0x2000)
+    hp = zr.zr_adamw(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)
+    assert L.zr_step_direct_range(None, 0, 1, 0.5, two, two, two, ctypes.byref(hp), None, None,
+                                  None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_rs_direct_norm_range(None, 0, 1, 0.5, two, None, None) == zr.ZR_ERR_INVALID_ARG
+    # the folded step: bucket, dtype, pointers, world cap, scale
+    assert L.zr_rs_adam_fused_acc(lay.handle, 3, two, two, zr.ZR_BF16, 0.5, two, two, two, ctypes.byref(hp),
+                                  None, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_rs_adam_fused_acc(lay.handle, 0, two, two, zr.ZR_FP32, 0.5, two, two, two, ctypes.byref(hp),
+                                  None, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_rs_adam_fused_acc(lay.handle, 0, odd, two, zr.ZR_BF16, 0.5, two, two, two, ctypes.byref(hp),
+                                  None, None, None) == zr.ZR_ERR_ALIGN
+    assert L.zr_rs_adam_fused_acc(lay.handle, 0, two, None, zr.ZR_BF16, 0.5, two, two, two, ctypes.byref(hp),
+                                  None, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_rs_adam_fused_acc(lay.handle, 0, two, two, zr.ZR_BF16, float("nan"), two, two, two,
+                                  ctypes.byref(hp), None, None, None) == zr.ZR_ERR_INVALID_ARG
+    big = zr.Layout([100, 200], 40, 1000)
+    forty = (ctypes.c_void_p * 40)(*([0x1000] * 40))
+    assert L.zr_rs_adam_fused_acc(big.handle, 0, forty, forty, zr.ZR_BF16, 0.5, forty, forty, forty,
+                                  ctypes.byref(hp), None, None, None) == zr.ZR_ERR_UNSUPPORTED
+    # the first micro-step
+    assert L.zr_grad_accumulate_first(None, None, zr.ZR_BF16, -1, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_grad_accumulate_first(None, None, zr.ZR_BF16, 0, None) == zr.ZR_OK
+    assert L.zr_grad_accumulate_first(ctypes.c_void_p(0x1002), ctypes.c_void_p(0x2000), zr.ZR_BF16, 10,
+                                      None) == zr.ZR_ERR_ALIGN
