@@ -119,6 +119,12 @@ WORKLOADS["irregular_prof"] = Workload(
     description="first 400 params of irregular_10k, world=16, bucket 2^24 (profiling size)")
 
 
+# The world sweep's fixed ~1B layout: the Llama 1.1B tensor list with bf16
+# gradients straight from one step (no micro-steps).
+WORKLOADS["llama_1p1b_bf16"] = dataclasses.replace(
+    WORKLOADS["llama_1p1b"], name="llama_1p1b_bf16", micro_steps=1,
+    description="Llama 1.1B shapes, bf16 grads of one step (the world sweep's layout)")
+
 # The Llama 1.1B micro-step path at profiling size: the first decoder layer's
 # nine tensors (44.0 M elements, one bucket), world 8, 4 bf16 micro-steps.
 WORKLOADS["llama_prof"] = Workload(
