@@ -341,8 +341,11 @@ int zr_rs_adam_fused_acc(const zr_layout *layout, int64_t bucket, const float *c
  * Steps 1 to 4 in one pass, without a bucket buffer. A direct plan records,
  * once, where every replica's gradient of every param of every bucket lives
  * (grads as for zr_bucket_pack; the tensors must stay allocated, at the same
- * addresses, while the plan is used) and how the bucket positions map to
- * params, in device memory the plan owns (8 bytes per replica and param, 8
+ * addresses, while the plan is used) and how the bucket's elements map to
+ * params (in flat order when the bucket holds a contiguous range of params,
+ * as under flat or backward arrival: the step needs no bucket buffer, so the
+ * order inside a bucket is free, and flat order makes its runs those of the
+ * partitions; in bucket order otherwise), in device memory the plan owns (8 bytes per replica and param, 8
  * per param, 36 per 256 bucket positions) plus a host copy of the param
  * offsets. zr_step_direct then does for bucket b what zr_bucket_pack followed
  * by zr_rs_adam_fused does, with identical results: each replica's slice of
