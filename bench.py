@@ -157,8 +157,11 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the device code (the kernels and what they include), which the
+    profiled DRAM traffic belongs to; host-side planning is not part of it."""
     h = hashlib.sha256()
-    for rel in ("zero_partition_aware_gb300/csrc/kernels.cu", "zero_partition_aware_gb300/csrc/zr_internal.h"):
+    for rel in ("zero_partition_aware_gb300/csrc/zr_kernels.cuh", "zero_partition_aware_gb300/csrc/zr_internal.h",
+                "include/zr.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
