@@ -620,9 +620,22 @@ def run_e2e(args, wl, grp, arenas, dplan, hp, stream, nranks, dist):
     e.record(stream)
     torch.cuda.synchronize()
     ms = dist.max(s.elapsed_time(e) / k)
+    # the floor: the same host-to-device copies alone, on the copy stream
+    cs.wait_stream(stream)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(cs)
+    for _ in range(k):
+        with torch.cuda.stream(cs):
+            for pairs in h2d_pairs:
+                for hs, dv in pairs:
+                    dv.copy_(hs, non_blocking=True)
+    e2.record(cs)
+    torch.cuda.synchronize()
+    ms_h2d = dist.max(s2.elapsed_time(e2) / k)
     del host
     return {"value": round(nranks * L.T / (ms / 1e3)), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": k,
+            "h2d_only_ms_per_step": round(ms_h2d, 3), "h2d_only_GB_per_s": round(h2d / (ms_h2d / 1e3) / 1e9, 1),
             "pipeline": "per bucket: H2D of its gradients, zr_step_direct, D2H of its bf16 params, on 3 streams"}
 
 
