@@ -385,6 +385,55 @@ def run_gpu(args, rank, nranks, local, dist):
                               "buffer sets, ordered by events"},
     }
 
+    # the unfused steps, one kernel each (reduce-scatter, AdamW over the partitions, the
+    # gather-cast) and the all-reduce reference path, per bucket after the planned pack
+    from zero_partition_aware_gb300 import zr as _zr
+    grads = grp.grad_shards()
+    ar_out = [torch.empty(max(grp.max_bucket, 1), dtype=torch.float32, device=device) for _ in range(wl.world)]
+    p_ar = _zr.PtrArray(ar_out)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def unfused_step(timed):
+        t = [0.0, 0.0, 0.0, 0.0]
+        for b in range(nbk):
+            pack(b)
+            e = [ev() for _ in range(4)]
+            e[0].record(stream)
+            _zr.zr_reduce_scatter_avg(L, b, grp._p_buckets, grp.scale, grp._p_grad, dtype=grp.zr_dtype, stream=stream)
+            e[1].record(stream)
+            _zr.zr_allreduce_avg(L, b, grp._p_buckets, grp.scale, p_ar, dtype=grp.zr_dtype, stream=stream)
+            e[2].record(stream)
+            timed.append(("rs", e[0], e[1]))
+            timed.append(("ar", e[1], e[2]))
+        e = [ev() for _ in range(3)]
+        e[0].record(stream)
+        _zr.zr_adam_shard_step(L, -1, grp._p_master, grp._p_m, grp._p_v, grp._p_grad, hp, stream=stream)
+        e[1].record(stream)
+        _zr.zr_gather_cast_bf16(L, grp._p_master, grp.param, stream=stream)
+        e[2].record(stream)
+        timed.append(("adam", e[0], e[1]))
+        timed.append(("cast", e[1], e[2]))
+
+    for _ in range(W_):
+        unfused_step([])
+    torch.cuda.synchronize()
+    marks = []
+    for _ in range(args.steps):
+        unfused_step(marks)
+    torch.cuda.synchronize()
+    tsum = {k: 0.0 for k in ("rs", "ar", "adam", "cast")}
+    for k, a, b_ in marks:
+        tsum[k] += a.elapsed_time(b_)
+    un_bytes = {"rs": L.P * (2 * wl.world + 4), "ar": L.P * (2 * wl.world + 4 * wl.world),
+                "adam": L.P * 28, "cast": L.P * 6}
+    unfused = {}
+    for k, name, bpp in (("rs", "reduce_scatter_avg", 2 * wl.world + 4), ("adam", "adam_shard_step", 28),
+                         ("cast", "gather_cast_bf16", 6), ("ar", "allreduce_avg", 6 * wl.world)):
+        g_ = gbs(un_bytes[k], tsum[k])
+        unfused[name] = {"ms_per_step": round(tsum[k] / args.steps, 4), "GB_per_s": round(g_, 1),
+                         "frac_of_peak": round(g_ / peak, 4), "bytes_per_param": bpp}
+    del ar_out, p_ar
+
     clipped = None
     if not args.no_clipped:
         # the step with the global gradient check before the update (two passes)
@@ -429,7 +478,7 @@ def run_gpu(args, rank, nranks, local, dist):
                               "one pass; consecutive buckets share launches)",
                       "l2": "no flush: every bucket's working set (~1 GB) exceeds the 129 MB L2",
                       "parallelism": f"replicas only x{nranks}"},
-           "roofline": roofline, "kernels": kernels, "two_kernel_step": two_kernel,
+           "roofline": roofline, "kernels": kernels, "two_kernel_step": two_kernel, "unfused_steps": unfused,
            "gpu_launches": int(launches), "clocks": clk}
     if clipped is not None:
         out["clipped_step"] = clipped
