@@ -318,6 +318,32 @@ def run_gpu(args, rank, nranks, local, dist):
     step_stats = timed_steps.last
     clk = clocks.stop()
 
+    # the same step captured once in a CUDA graph and replayed
+    graph_ms = None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            grp.step_direct(dplan, hp)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            grp.step_direct(dplan, hp)
+        for _ in range(2):
+            cg.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            cg.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        graph_ms = dist.max(g0.elapsed_time(g1) / args.steps)
+        del cg
+    except RuntimeError as e:  # reported, not fatal: the eager step is the measured one
+        graph_ms = f"capture failed: {e}"
+
     # the same step with one launch per bucket (zr_step_direct), as buckets reduced while backward fills them
     for _ in range(W_):
         for b in range(nbk):
@@ -368,6 +394,8 @@ def run_gpu(args, rank, nranks, local, dist):
         "rs_direct": {"ms_per_step": round(t_direct / args.steps, 4), "GB_per_s": round(direct_gbs, 1),
                       "frac_of_peak": round(direct_gbs / peak, 4), "bytes_per_param": 2 * wl.world + 26,
                       "launches_per_step": launches_per_step},
+        "rs_direct_graph": {"ms_per_step": round(graph_ms, 4) if isinstance(graph_ms, float) else graph_ms,
+                            "how": "the same step captured once in a CUDA graph, replayed"},
         "rs_direct_per_bucket": {"ms_per_step": round(ms_pb, 4), "params_per_s": round(nranks * L.T / (ms_pb / 1e3)),
                                  "GB_per_s": round(pb_gbs, 1), "frac_of_peak": round(pb_gbs / peak, 4),
                                  "launches_per_step": round(launches_pb / args.steps)},
