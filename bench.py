@@ -404,9 +404,13 @@ def run_gpu(args, rank, nranks, local, dist):
         "ms_per_step": round(ms_two, 4), "params_per_s": round(nranks * L.T / (ms_two / 1e3)),
         "launches_per_step": round(launches_two / args.steps),
         "bucket_pack": {"ms_per_step": round(t_pack / args.steps, 4), "GB_per_s": round(pack_gbs, 1),
-                        "frac_of_peak": round(pack_gbs / peak, 4), "bytes_per_param": 4 * wl.world},
+                        "frac_of_peak": round(pack_gbs / peak, 4), "bytes_per_param": 4 * wl.world,
+                        "traffic_per_replica_element": (profiled_traffic("bucket_pack_bf16_w16") or {}).get(
+                            "dram_bytes_per_element") if wl.world == 16 else None},
         "rs_adam_fused": {"ms_per_step": round(t_fused / args.steps, 4), "GB_per_s": round(fused_gbs, 1),
-                          "frac_of_peak": round(fused_gbs / peak, 4), "bytes_per_param": 2 * wl.world + 26},
+                          "frac_of_peak": round(fused_gbs / peak, 4), "bytes_per_param": 2 * wl.world + 26,
+                          "traffic_per_element": (profiled_traffic("rs_adam_fused_bf16_w16") or {}).get(
+                              "dram_bytes_per_element") if wl.world == 16 else None},
         "overlapped": {"ms_per_step": round(ms_ov, 4), "params_per_s": round(nranks * L.T / (ms_ov / 1e3)),
                        "GB_per_s": round(gbs(pack_bytes + fused_bytes, ms_ov * args.steps), 1),
                        "how": "pack of bucket b+1 on a second stream while bucket b is reduced; two bucket "
