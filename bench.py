@@ -724,15 +724,18 @@ def run_e2e(args, wl, grp, arenas, dplan, hp, stream, nranks, dist):
 # the CPU oracle (cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(wl, n_elems, seed=0):
+def oracle_sample(wl, n_elems, seed=0, skip_larger=False):
     """A bounded sample of the workload on the host: the first bucket's leading
-    params (at most n_elems elements) with their state, drawn on the CPU."""
+    params (at most n_elems elements; with skip_larger, params of more than
+    n_elems elements are passed over) with their state, drawn on the CPU."""
     import torch
     import oracle
     from zero_partition_aware_gb300 import workloads as W
     numel = []
     tot = 0
     for n in wl.numel:
+        if skip_larger and n > n_elems:
+            continue
         if tot + n > n_elems and numel:
             break
         numel.append(int(n))
@@ -788,6 +791,51 @@ def cpu_baseline(wl, budget_s):
             "seconds": round(dt, 2)}
 
 
+def cpu_baseline_all_cores(wl, budget_s):
+    """The oracle as it stands on every host core: one thread per core, each
+    with its own copy of one bounded sample (leading params of at most
+    2^24 / threads elements, larger params passed over) and its own state,
+    re-running pack + fused step over the same wall-clock window. The oracle
+    is C called through ctypes, which releases the GIL for each call, so the
+    threads run in parallel; no process is forked. Throughput = elements of
+    all completed steps / the window."""
+    import threading
+    import oracle
+    oracle.build()
+    n_thr = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    scale = float(np.float32(1.0 / wl.world))
+    lay, grads, p, m, v = oracle_sample(wl, max(min(wl.bucket, 1 << 24) // n_thr, 1), skip_larger=True)
+    copy = lambda x: [copy(y) for y in x] if isinstance(x, list) else x.copy()
+    work = [(copy(grads), copy(p), copy(m), copy(v)) for _ in range(n_thr)]
+    done = [0] * n_thr
+    go = threading.Barrier(n_thr + 1)
+    t_end = [0.0]
+
+    def run(i):
+        g, pp, mm, vv = work[i]
+        go.wait()
+        while time.perf_counter() < t_end[0]:
+            oracle_step(lay, g, pp, mm, vv, wl.adam, scale, micro=wl.micro_steps > 1)
+            done[i] += 1
+
+    ths = [threading.Thread(target=run, args=(i,)) for i in range(n_thr)]
+    for t in ths:
+        t.start()
+    t0 = time.perf_counter()
+    t_end[0] = t0 + budget_s
+    go.wait()
+    for t in ths:
+        t.join()
+    dt = time.perf_counter() - t0
+    return {"value": round(sum(done) * lay.T / dt), "unit": UNIT, "cores": n_thr, "kind": "oracle",
+            "sample": f"{n_thr} threads, each its own copy of {lay.n_params} params ({lay.T} elements) of "
+                      f"{wl.name} (leading params of at most {max(min(wl.bucket, 1 << 24) // n_thr, 1)} elements), "
+                      f"world {wl.world}: "
+                      + (f"{wl.micro_steps} micro-step accumulations + " if wl.micro_steps > 1 else "")
+                      + f"pack + fused step, {sum(done)} steps completed in {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
 def run_reference(args):
     from zero_partition_aware_gb300 import workloads as W
     import oracle
@@ -837,6 +885,7 @@ def main():
     if rank == 0:
         if nranks == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(W_lookup(args), args.cpu_seconds)
+            out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(W_lookup(args), args.cpu_seconds / 2)
         print(json.dumps(out), flush=True)
     dist.close()
     return 0
