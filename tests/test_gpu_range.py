@@ -156,3 +156,56 @@ def test_range_subsets_and_bad_ranges(zr):
         with pytest.raises(zr.ZrError):
             zr.zr_step_direct_range(plan, first, count, 0.125, P_, M_, V_, hp, param)
     zr.zr_step_direct_range(plan, 2, 0, 0.125, P_, M_, V_, hp, param)  # empty range: nothing to do
+
+
+@pytest.mark.parametrize("world,s_phase,q_phase", [(8, 0, 0), (8, 1, 3), (16, 2, 6), (16, 3, 5), (40, 1, 2)])
+def test_flat_view_shards_anchor_on_the_params(zr, world, s_phase, q_phase):
+    """Master, m and v as views of one flat buffer each (partition r at rS, the
+    buffer s_phase fp32 elements past a 16-byte boundary), the bf16 params
+    q_phase elements past one, S odd: tiles are anchored on the params where
+    the phases agree modulo 4 elements. The direct range step (world <= 32) and
+    the per-bucket fused step from packed buckets must equal the oracle bit for
+    bit."""
+    rng = np.random.default_rng(world * 100 + s_phase * 10 + q_phase)
+    numel = W.random_numels(rng, 60, 1, 40_000)
+    lay = oracle.layout(numel, world, 200_000)
+    if lay.S % 2 == 0:  # an odd S puts the partitions at every phase; world more elements add one to S
+        numel[-1] += world
+        lay = oracle.layout(numel, world, 200_000)
+    assert lay.S % 2 == 1
+    zl = zr.Layout(numel, world, 200_000)
+    raw = [[(rng.standard_normal(k) * 1e-2).astype(np.float32) for k in numel] for _ in range(world)]
+    grads = [[oracle.f32_to_bf16(x) for x in row] for row in raw]
+    keep = []
+    rows = [[_dev(g, int(rng.integers(0, 8)), keep) for g in row] for row in grads]
+    flat = lambda std: np.concatenate([(rng.standard_normal(lay.T) * std).astype(np.float32),
+                                       np.zeros(lay.P - lay.T, np.float32)])
+    state = [flat(0.02), np.abs(flat(1e-4)), np.abs(flat(1e-4))]
+    hp = W.AdamW(step=4)
+    scale = float(np.float32(1.0 / world))
+    rp, rm, rv = ([a.copy() for a in np.split(x, world)] for x in state)
+    rparam = np.zeros(lay.P, np.uint16)
+    for b in range(lay.n_buckets):
+        oracle.rs_adam_fused(lay, b, oracle.bucket_pack(lay, b, grads), scale, rp, rm, rv, hp, rparam)
+    for packed in ((False, True) if world <= 32 else (True,)):  # the direct step takes world <= 32
+        views = []
+        for x in state:
+            buf = _dev(x, s_phase, keep)
+            views.append([buf[r * lay.S:(r + 1) * lay.S] for r in range(world)])
+        P_, M_, V_ = views
+        qbuf = torch.zeros(lay.P + 8, dtype=torch.bfloat16, device="cuda")
+        param = qbuf[q_phase:q_phase + lay.P]
+        param.fill_(float("nan"))
+        if packed:
+            for b in range(lay.n_buckets):
+                _, nb = lay.bucket(b)
+                bk = [torch.empty(nb, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+                zr.zr_bucket_pack(zl, b, rows, bk)
+                zr.zr_rs_adam_fused(zl, b, bk, scale, P_, M_, V_, hp, param)
+        else:
+            zr.zr_step_direct_range(zr.DirectPlan(zl, rows), 0, lay.n_buckets, scale, P_, M_, V_, hp, param)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(param), rparam), packed
+        for r in range(world):
+            for a, b_ in ((P_[r], rp[r]), (M_[r], rm[r]), (V_[r], rv[r])):
+                assert np.array_equal(_bits(a), b_.view(np.uint32)), (packed, r)

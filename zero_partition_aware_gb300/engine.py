@@ -2,7 +2,8 @@
 
 ``DPGroup`` owns what each of the N ranks would hold under ZeRO stage 1/2
 ("Megatron-LM 分布式训练（四）" §"ZeRO 各档"; "DeepSpeed ZeRO 通信优化深度解析"
-§二, §三.3): its fp32 master, m and v partition of S elements, its IPG bucket
+§二, §三.3): its fp32 master, m and v partition of S elements (views of one
+flat buffer per state, partition r at offset rS), its IPG bucket
 buffer (reused bucket after bucket, as stage 2 releases it once the slice is
 reduced), and the full bf16 parameter buffer the all-gather refreshes. One
 ``step`` runs, for every bucket in order, the packing of each rank's
@@ -31,9 +32,11 @@ class DPGroup:
         L = self.layout
         S = L.S
         f32 = dict(dtype=torch.float32, device=self.device)
-        self.master = [torch.zeros(S, **f32) for _ in range(world)]
-        self.m = [torch.zeros(S, **f32) for _ in range(world)]
-        self.v = [torch.zeros(S, **f32) for _ in range(world)]
+        # Each state is one flat [P] buffer laid out like the parameters, partition
+        # r its view at r*S: partition elements keep the parameters' 16-byte
+        # phases, so the fused kernels store the bf16 params in aligned chunks.
+        self._flat_state = [torch.zeros(max(L.P, 1), **f32) for _ in range(3)]
+        self.master, self.m, self.v = ([buf[r * S:(r + 1) * S] for r in range(world)] for buf in self._flat_state)
         self.param = torch.zeros(max(L.P, 1), dtype=torch.bfloat16, device=self.device)
         self.max_bucket = max((L.bucket(b)[1] for b in range(L.n_buckets)), default=0)
         self.buckets: List[torch.Tensor] = []
@@ -163,8 +166,9 @@ class DPGroup:
         first use: the two-pass step keeps the whole averaged gradient until
         the check has seen all of it (the partition gradient of stage 2)."""
         if getattr(self, "_grad", None) is None:
-            self._grad = [torch.zeros(self.layout.S, dtype=torch.float32, device=self.device)
-                          for _ in range(self.world)]
+            S = self.layout.S  # views of one flat buffer, like master, m and v
+            buf = torch.zeros(max(self.layout.P, 1), dtype=torch.float32, device=self.device)
+            self._grad = [buf[r * S:(r + 1) * S] for r in range(self.world)]
             self._p_grad = zr.PtrArray(self._grad)
             self.check = zr.GradCheck()
         return self._grad
