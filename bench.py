@@ -794,7 +794,8 @@ def cpu_baseline(wl, budget_s):
 def cpu_baseline_all_cores(wl, budget_s):
     """The oracle as it stands on every host core: one thread per core, each
     with its own copy of one bounded sample (leading params of at most
-    2^24 / threads elements, larger params passed over) and its own state,
+    2^24 / threads elements, or of the first bucket up to 2^20 if that is more;
+    larger params passed over) and its own state,
     re-running pack + fused step over the same wall-clock window. The oracle
     is C called through ctypes, which releases the GIL for each call, so the
     threads run in parallel; no process is forked. Throughput = elements of
@@ -804,7 +805,8 @@ def cpu_baseline_all_cores(wl, budget_s):
     oracle.build()
     n_thr = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     scale = float(np.float32(1.0 / wl.world))
-    lay, grads, p, m, v = oracle_sample(wl, max(min(wl.bucket, 1 << 24) // n_thr, 1), skip_larger=True)
+    cap = max(min(wl.bucket, 1 << 24) // n_thr, min(wl.bucket, 1 << 20))
+    lay, grads, p, m, v = oracle_sample(wl, cap, skip_larger=True)
     copy = lambda x: [copy(y) for y in x] if isinstance(x, list) else x.copy()
     work = [(copy(grads), copy(p), copy(m), copy(v)) for _ in range(n_thr)]
     done = [0] * n_thr
@@ -829,7 +831,7 @@ def cpu_baseline_all_cores(wl, budget_s):
     dt = time.perf_counter() - t0
     return {"value": round(sum(done) * lay.T / dt), "unit": UNIT, "cores": n_thr, "kind": "oracle",
             "sample": f"{n_thr} threads, each its own copy of {lay.n_params} params ({lay.T} elements) of "
-                      f"{wl.name} (leading params of at most {max(min(wl.bucket, 1 << 24) // n_thr, 1)} elements), "
+                      f"{wl.name} (leading params of at most {cap} elements), "
                       f"world {wl.world}: "
                       + (f"{wl.micro_steps} micro-step accumulations + " if wl.micro_steps > 1 else "")
                       + f"pack + fused step, {sum(done)} steps completed in {dt:.1f} s",
