@@ -359,18 +359,27 @@ def run_gpu(args, rank, nranks, local, dist):
     torch.cuda.synchronize()
     ms_two, t_pack, t_fused, launches_two = timed_steps(args, nbk, pack, fused, stream, dist)
 
+    # the same packed buckets reduced in flat order: the direct kernel over their param slices
+    reduce_flat = lambda b: grp.reduce_packed(b, hp, stream=stream)
+    for _ in range(W_):
+        for b in range(nbk):
+            pack(b)
+            reduce_flat(b)
+    torch.cuda.synchronize()
+    ms_two_f, _, t_red_f, _ = timed_steps(args, nbk, pack, reduce_flat, stream, dist)
+
     # the same two kernels with packing overlapped: bucket b+1 packed on a second stream while b is reduced
     plans2 = grp.overlap_plans(table)
     side = torch.cuda.Stream()
     for _ in range(W_):
-        grp.step_overlapped(plans2, hp, stream=stream, side_stream=side)
+        grp.step_overlapped(plans2, hp, stream=stream, side_stream=side, flat_order=True)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
     ev0.record(stream)
     for _ in range(args.steps):
-        grp.step_overlapped(plans2, hp, stream=stream, side_stream=side)
+        grp.step_overlapped(plans2, hp, stream=stream, side_stream=side, flat_order=True)
     ev1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
@@ -411,10 +420,16 @@ def run_gpu(args, rank, nranks, local, dist):
                           "frac_of_peak": round(fused_gbs / peak, 4), "bytes_per_param": 2 * wl.world + 26,
                           "traffic_per_element": (profiled_traffic("rs_adam_fused_bf16_w16") or {}).get(
                               "dram_bytes_per_element") if wl.world == 16 else None},
+        "reduced_in_flat_order": {
+            "ms_per_step": round(ms_two_f, 4), "params_per_s": round(nranks * L.T / (ms_two_f / 1e3)),
+            "reduce_ms_per_step": round(t_red_f / args.steps, 4),
+            "reduce_frac_of_peak": round(gbs(fused_bytes, t_red_f) / peak, 4),
+            "how": "the same packed buckets, each reduced by zr_step_direct over a plan whose gradients are the "
+                   "bucket buffers' param slices (DPGroup.reduce_packed)"},
         "overlapped": {"ms_per_step": round(ms_ov, 4), "params_per_s": round(nranks * L.T / (ms_ov / 1e3)),
                        "GB_per_s": round(gbs(pack_bytes + fused_bytes, ms_ov * args.steps), 1),
-                       "how": "pack of bucket b+1 on a second stream while bucket b is reduced; two bucket "
-                              "buffer sets, ordered by events"},
+                       "how": "pack of bucket b+1 on a second stream while bucket b is reduced in flat order "
+                              "(DPGroup.reduce_packed); two bucket buffer sets, ordered by events"},
     }
 
     # the unfused steps, one kernel each (reduce-scatter, AdamW over the partitions, the

@@ -74,19 +74,23 @@ def test_from_host_equals_device_resident(mods, world, n, hi, B):
             assert np.array_equal(_bits(a), _bits(b)), r
 
 
+@pytest.mark.parametrize("flat_order", [False, True], ids=["fused", "flat_order_reverse_arrival"])
 @pytest.mark.parametrize("world,n,hi,B", [(4, 40, 30_000, 60_000), (16, 120, 200_000, 1 << 21), (8, 5, 1000, 1)])
-def test_overlapped_pack_and_fused_equal_the_sequential_step(mods, world, n, hi, B):
+def test_overlapped_pack_and_fused_equal_the_sequential_step(mods, world, n, hi, B, flat_order):
     """Packing bucket b+1 on a second stream while bucket b is reduced (two
-    bucket buffer sets) gives the sequential step's results bit for bit."""
+    bucket buffer sets) gives the sequential step's results bit for bit; with
+    flat_order, under backward arrival, each bucket is reduced by the direct
+    kernel over the buffer set's param slices."""
     engine, zr = mods
     rng = np.random.default_rng(100 + world)
     numel = W.random_numels(rng, n, 1, hi)
     wl = W.Workload("ov", tuple(numel), world, B, ("normal", 1e-2), 0.02, ("absnormal", 1e-4), W.AdamW(step=2))
     inp = W.draw_inputs(wl, "cuda", seed=world)
     hp = W.AdamW(step=2)
+    arrival = list(range(n - 1, -1, -1)) if flat_order else None
     groups = []
     for _ in range(2):
-        g = engine.DPGroup(numel, world, B, device="cuda")
+        g = engine.DPGroup(numel, world, B, device="cuda", arrival=arrival)
         g.load_flat(inp["master"], inp["m"], inp["v"])
         groups.append(g)
     L = groups[0].layout
@@ -97,7 +101,7 @@ def test_overlapped_pack_and_fused_equal_the_sequential_step(mods, world, n, hi,
     a.step(ta, hp, plan=a.pack_plan(ta))
     plans = b.overlap_plans(tb)
     for _ in range(2):  # twice: the second step reuses both buffer sets
-        b.step_overlapped(plans, hp)
+        b.step_overlapped(plans, hp, flat_order=flat_order)
     a.step(ta, hp, plan=a.pack_plan(ta))
     torch.cuda.synchronize()
     assert np.array_equal(_bits(a.param[: L.P]), _bits(b.param[: L.P]))

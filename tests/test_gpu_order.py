@@ -152,3 +152,45 @@ def test_step_under_order(zr, world, seed, n, hi, B, kind, path):
         assert np.array_equal(_bits(P_[r]), rp[r].view(np.uint32)), r
         assert np.array_equal(_bits(M_[r]), rm[r].view(np.uint32)), r
         assert np.array_equal(_bits(V_[r]), rv[r].view(np.uint32)), r
+
+
+@pytest.mark.parametrize("kind", ["reverse", "random", "flat"])
+@pytest.mark.parametrize("world,seed,n,hi,B", [(8, 11, 40, 6000, 20000), (16, 12, 80, 9000, 100_000),
+                                               (3, 13, 12, 3000, 1)])
+def test_packed_buckets_reduced_in_flat_order(zr, kind, world, seed, n, hi, B):
+    """DPGroup.step_packed: each bucket packed in arrival order, then reduced by
+    the direct step over the bucket buffers' param slices (flat order); equal
+    to the oracle's pack + fused step bit for bit."""
+    from zero_partition_aware_gb300.engine import DPGroup
+    rng = np.random.default_rng(900 + seed)
+    numel = W.random_numels(rng, n, 1, hi)
+    order = None if kind == "flat" else _order(kind, rng, n)
+    lay = oracle.layout(numel, world, B, order=order)
+    grads = [[W.bf16_bits(torch.from_numpy((rng.standard_normal(k) * 1e-2).astype(np.float32)).to(torch.bfloat16))
+              for k in numel] for _ in range(world)]
+    keep, rows = [], []
+    for row in grads:
+        r_ = []
+        for g in row:
+            base, v = _dev(g, int(rng.integers(0, 8)))
+            keep.append(base)
+            r_.append(v)
+        rows.append(r_)
+    flat = lambda std: (rng.standard_normal(lay.T) * std).astype(np.float32)
+    master, m, v = flat(0.02), np.abs(flat(1e-4)), np.abs(flat(1e-4))
+    hp = W.AdamW(step=3)
+    grp = DPGroup(numel, world, B, arrival=order)
+    grp.load_flat(*(torch.from_numpy(x).cuda() for x in (master, m, v)))
+    grp.param.fill_(float("nan"))
+    plan = grp.pack_plan(grp.grad_table(rows))
+    grp.step_packed(plan, hp)
+    torch.cuda.synchronize()
+    pad = lambda x: np.concatenate([x, np.zeros(lay.P - lay.T, np.float32)])
+    rp, rm, rv = ([a.copy() for a in np.split(pad(x), world)] for x in (master, m, v))
+    rparam = np.zeros(lay.P, np.uint16)
+    for b in range(lay.n_buckets):
+        oracle.rs_adam_fused(lay, b, oracle.bucket_pack(lay, b, grads), grp.scale, rp, rm, rv, hp, rparam)
+    assert np.array_equal(_bits(grp.param[: lay.P]), rparam)
+    for r in range(world):
+        for a, b_ in ((grp.master[r], rp[r]), (grp.m[r], rm[r]), (grp.v[r], rv[r])):
+            assert np.array_equal(_bits(a), b_.view(np.uint32)), r

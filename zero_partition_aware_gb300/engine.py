@@ -14,6 +14,7 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence
 
+import numpy as np
 import torch
 
 from . import zr
@@ -96,6 +97,39 @@ class DPGroup:
                 self.pack(b, grad_table, stream)
             self.fused(b, hp, stream=stream)
 
+    def bucket_plan(self, buffer_set: int = 0) -> zr.DirectPlan:
+        """A direct-step plan whose gradients are bucket buffers (set 0: the
+        group's own, set 1: step_overlapped's second set): replica k's gradient
+        of param i is its slice of bucket buffer k, at the param's offset inside
+        its bucket. Once bucket b is packed, zr_step_direct with this plan
+        reduces it in flat order, whatever order the params arrived in. Built
+        on first use; the bucket buffers stay."""
+        plans = self.__dict__.setdefault("_bucket_plans", {})
+        if buffer_set not in plans:
+            bufs = self.buckets if buffer_set == 0 else getattr(self, "_buckets2", None)
+            if not bufs:
+                raise ValueError(f"the group has no bucket buffer set {buffer_set}")
+            L = self.layout
+            sl = L.slices()
+            boff = np.zeros(L.n_params, np.int64)
+            boff[sl[:, 0]] = sl[:, 4] - sl[:, 3]  # bucket offset of the slice - its offset in the param
+            es = bufs[0].element_size()
+            addrs = [int(buf.data_ptr()) + int(o) * es for buf in bufs for o in boff]
+            plans[buffer_set] = zr.DirectPlan(L, zr.PtrArray(addrs), dtype=self.zr_dtype)
+        return plans[buffer_set]
+
+    def reduce_packed(self, b: int, hp, write_param: bool = True, stream=None, buffer_set: int = 0) -> None:
+        """Steps 2-4 of packed bucket b, read from a bucket buffer set in flat
+        order (zr_step_direct over bucket_plan): the same result as fused()."""
+        self.direct(b, self.bucket_plan(buffer_set), hp, write_param=write_param, stream=stream)
+
+    def step_packed(self, plan: zr.PackPlan, hp, stream=None) -> None:
+        """The two-kernel step with the reduction in flat order: every bucket
+        packed by its plan, then reduced by reduce_packed."""
+        for b in range(self.layout.n_buckets):
+            self.pack_planned(b, plan, stream)
+            self.reduce_packed(b, hp, stream=stream)
+
     def overlap_plans(self, grad_table: zr.PtrArray):
         """Two pack plans over two sets of bucket buffers, for step_overlapped:
         bucket b+1 is packed into one set while bucket b is reduced from the
@@ -107,14 +141,15 @@ class DPGroup:
         return (zr.PackPlan(self.layout, grad_table, self._p_buckets, dtype=self.zr_dtype),
                 zr.PackPlan(self.layout, grad_table, self._p_buckets2, dtype=self.zr_dtype))
 
-    def step_overlapped(self, plans, hp, stream=None, side_stream=None) -> None:
+    def step_overlapped(self, plans, hp, stream=None, side_stream=None, flat_order: bool = False) -> None:
         """The two-kernel step with packing and reduction overlapped
         ("DeepSpeed ZeRO 通信优化深度解析" §四, §五 overlap_comm: the copy into the
         IPG bucket and the reduction of the previous bucket run on different
         streams): bucket b+1 is packed on side_stream into one buffer set while
         the fused step reduces bucket b from the other. Events order each
         buffer's reuse; nothing waits on the device. `stream` waits for all
-        of it at the end."""
+        of it at the end. flat_order: each bucket reduced by reduce_packed
+        instead of the fused kernel."""
         cur = stream or torch.cuda.current_stream(self.device)
         side = side_stream or torch.cuda.Stream(self.device)
         nb = self.layout.n_buckets
@@ -135,7 +170,10 @@ class DPGroup:
                     zr.zr_bucket_pack_planned(plans[(b + 1) % 2], b + 1, stream=side)
                     packed[b + 1].record(side)
             cur.wait_event(packed[b])
-            self.fused(b, hp, bucket_in=sets[b % 2], stream=cur)
+            if flat_order:
+                self.reduce_packed(b, hp, stream=cur, buffer_set=b % 2)
+            else:
+                self.fused(b, hp, bucket_in=sets[b % 2], stream=cur)
             used[b].record(cur)
         cur.wait_stream(side)
 
