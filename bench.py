@@ -728,10 +728,39 @@ def run_e2e(args, wl, grp, arenas, dplan, hp, stream, nranks, dist):
     e2.record(cs)
     torch.cuda.synchronize()
     ms_h2d = dist.max(s2.elapsed_time(e2) / k)
+    # the parameter read-back alone, then both directions' copies at once (no compute)
+    param = grp.param[: L.P]
+    ds.wait_stream(stream)
+    s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s3.record(ds)
+    with torch.cuda.stream(ds):
+        for _ in range(k):
+            out_host.copy_(param, non_blocking=True)
+    e3.record(ds)
+    torch.cuda.synchronize()
+    ms_d2h = dist.max(s3.elapsed_time(e3) / k)
+    s4, e4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s4.record(stream)
+    cs.wait_stream(stream)
+    ds.wait_stream(stream)
+    for _ in range(k):
+        with torch.cuda.stream(cs):
+            for pairs in h2d_pairs:
+                for hs, dv in pairs:
+                    dv.copy_(hs, non_blocking=True)
+        with torch.cuda.stream(ds):
+            out_host.copy_(param, non_blocking=True)
+    stream.wait_stream(cs)
+    stream.wait_stream(ds)
+    e4.record(stream)
+    torch.cuda.synchronize()
+    ms_both = dist.max(s4.elapsed_time(e4) / k)
     del host
     return {"value": round(nranks * L.T / (ms / 1e3)), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": k,
             "h2d_only_ms_per_step": round(ms_h2d, 3), "h2d_only_GB_per_s": round(h2d / (ms_h2d / 1e3) / 1e9, 1),
+            "d2h_only_ms_per_step": round(ms_d2h, 3), "d2h_only_GB_per_s": round(d2h / (ms_d2h / 1e3) / 1e9, 1),
+            "copies_only_ms_per_step": round(ms_both, 3),
             "pipeline": "per bucket: H2D of its gradients, zr_step_direct, D2H of its bf16 params, on 3 streams"}
 
 
