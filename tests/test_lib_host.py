@@ -274,3 +274,24 @@ def test_range_folded_and_first_validate_before_launch(zr):
     assert L.zr_grad_accumulate_first(None, None, zr.ZR_BF16, 0, None) == zr.ZR_OK
     assert L.zr_grad_accumulate_first(ctypes.c_void_p(0x1002), ctypes.c_void_p(0x2000), zr.ZR_BF16, 10,
                                       None) == zr.ZR_ERR_ALIGN
+
+
+@pytest.mark.parametrize("kind", ["flat", "reverse", "random"])
+def test_param_bucket_offsets_match_the_oracle(zr, kind):
+    """The offsets the flat-order reduction of packed buckets points into: each
+    param's first element inside its bucket, as the oracle's layout places it
+    (the flat offset minus the bucket's flat start, or its bucket position)."""
+    from zero_partition_aware_gb300.engine import param_bucket_offsets
+    rng = np.random.default_rng(sum(map(ord, kind)))
+    numel = W.random_numels(rng, 300, 1, 50_000)
+    n = len(numel)
+    order = None if kind == "flat" else (list(range(n - 1, -1, -1)) if kind == "reverse"
+                                         else [int(x) for x in rng.permutation(n)])
+    for world, B in ((8, 200_000), (16, 1), (3, 1 << 22)):
+        got = param_bucket_offsets(zr.Layout(numel, world, B, arrival=order))
+        lay = oracle.layout(numel, world, B, order=order)
+        if order is None:
+            want = lay.offset - lay.bucket_range[lay.bucket_of, 0]
+        else:
+            want = lay.bucket_pos
+        assert np.array_equal(got, want), (world, B)

@@ -20,6 +20,15 @@ import torch
 from . import zr
 
 
+def param_bucket_offsets(layout: zr.Layout) -> np.ndarray:
+    """[n_params]: where each param's first element sits inside its bucket (any
+    slice's bucket offset minus its offset in the param)."""
+    sl = layout.slices()
+    out = np.zeros(layout.n_params, np.int64)
+    out[sl[:, 0]] = sl[:, 4] - sl[:, 3]
+    return out
+
+
 class DPGroup:
     def __init__(self, numel: Sequence[int], world: int,
                  reduce_bucket_size: int = zr.ZR_DEFAULT_REDUCE_BUCKET_SIZE,
@@ -110,9 +119,7 @@ class DPGroup:
             if not bufs:
                 raise ValueError(f"the group has no bucket buffer set {buffer_set}")
             L = self.layout
-            sl = L.slices()
-            boff = np.zeros(L.n_params, np.int64)
-            boff[sl[:, 0]] = sl[:, 4] - sl[:, 3]  # bucket offset of the slice - its offset in the param
+            boff = param_bucket_offsets(L)
             es = bufs[0].element_size()
             addrs = [int(buf.data_ptr()) + int(o) * es for buf in bufs for o in boff]
             plans[buffer_set] = zr.DirectPlan(L, zr.PtrArray(addrs), dtype=self.zr_dtype)
