@@ -157,13 +157,19 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the device code (the kernels and what they include), which the
-    profiled DRAM traffic belongs to; host-side planning is not part of it."""
+    """Hash of the device code (the kernels and what they include, comments
+    removed), which the profiled DRAM traffic belongs to; host-side planning
+    and comments are not part of it."""
+    import re
     h = hashlib.sha256()
     for rel in ("zero_partition_aware_gb300/csrc/zr_kernels.cuh", "zero_partition_aware_gb300/csrc/zr_internal.h",
                 "include/zr.h"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+        h.update(src.encode())
     return h.hexdigest()[:16]
 
 

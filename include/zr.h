@@ -39,7 +39,12 @@
  *    errors of the asynchronous execution surface at the caller's next
  *    synchronisation.
  *  - Device pointers need only element alignment (2 bytes for bf16, 4 for
- *    fp32); otherwise ZR_ERR_ALIGN. Any 16-byte phase is accepted.
+ *    fp32); otherwise ZR_ERR_ALIGN. Any 16-byte phase is accepted. The fused
+ *    steps run fastest when partition r of master, m and v (and of the shard
+ *    gradient) starts at the same 16-byte phase, modulo 4 elements, as element
+ *    r*S of param_bf16: as views at offset r*S of flat [P] buffers laid out
+ *    like the parameters. Their tiles then start every stream on a 16-byte
+ *    boundary; results are the same either way.
  *  - Outputs must not overlap inputs except where an argument is in/out.
  */
 #ifndef ZR_H
