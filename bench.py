@@ -156,20 +156,24 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments, blank lines and trailing blanks
+    (the sources have no comment markers inside string literals)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
     """Hash of the device code (the kernels and what they include, comments
     removed), which the profiled DRAM traffic belongs to; host-side planning
     and comments are not part of it."""
-    import re
     h = hashlib.sha256()
     for rel in ("zero_partition_aware_gb300/csrc/zr_kernels.cuh", "zero_partition_aware_gb300/csrc/zr_internal.h",
                 "include/zr.h"):
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
-            src = f.read()
-        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-        src = re.sub(r"//[^\n]*", "", src)
-        src = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
-        h.update(src.encode())
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -40,3 +40,12 @@ def test_single_thread_leg():
     from zero_partition_aware_gb300 import workloads as W
     d = bench.cpu_baseline(W.WORKLOADS["tiny"], 0.3)
     assert d["cores"] == 1 and d["value"] > 0 and d["kind"] == "oracle"
+
+
+def test_traffic_hash_ignores_comments_not_code():
+    bench = _bench()
+    a = "int f(int x) {\n    return x + 1;  // one\n}\n"
+    b = "/* doc\n   more */\nint f(int x) {\n\n    return x + 1;\n}   \n// end\n"
+    c = "int f(int x) {\n    return x + 2;\n}\n"
+    assert bench.code_only(a) == bench.code_only(b) != bench.code_only(c)
+    assert len(bench.kernel_source_hash()) == 16
