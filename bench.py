@@ -166,14 +166,16 @@ def code_only(src: str) -> str:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the device code (the kernels and what they include, comments
-    removed), which the profiled DRAM traffic belongs to; host-side planning
-    and comments are not part of it."""
+    """Hash of what the profiled DRAM traffic belongs to: the device code, the
+    host code that plans and launches it (grids, shared memory, launch shapes)
+    and the compiler flags, with comments removed; comment changes leave it."""
+    from zero_partition_aware_gb300 import build as zb
     h = hashlib.sha256()
     for rel in ("zero_partition_aware_gb300/csrc/zr_kernels.cuh", "zero_partition_aware_gb300/csrc/zr_internal.h",
-                "include/zr.h"):
+                "zero_partition_aware_gb300/csrc/kernels.cu", "include/zr.h"):
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             h.update(code_only(f.read()).encode())
+    h.update(" ".join(zb.ARCH + zb.COMMON_FLAGS).encode())
     return h.hexdigest()[:16]
 
 

@@ -228,15 +228,17 @@ int zr_bucket_pack_planned(const zr_pack_plan *plan, int64_t bucket, zr_stream s
 /*
  * zr_bucket_pack without any device allocation, for callers that cannot call
  * cudaMalloc: for example a framework that serves all device memory from its
- * own pool and holds the process to a fixed budget, or a step that must not
- * take the implicit device synchronisation an allocation or free may bring.
- * The pages have no counterpart to this; it is a deployment convenience.
- * Same arguments and results as zr_bucket_pack, in one launch: the bucket's
- * segment table (one segment per replica and param, contiguous params merged,
- * plus the padding) is copied with cudaMemcpyAsync into a fixed table inside
- * the library's device code, at most 8192 segments (384 KB, held on every GPU
- * that loads the library until exit); a bigger bucket returns
- * ZR_ERR_UNSUPPORTED. The first call on a device looks the table's address up
+ * own pool and holds the process to a fixed budget, where an allocation behind
+ * its back would break the budget or fail. The pages have no counterpart to
+ * this; it is a deployment convenience.
+ * Same arguments and results as zr_bucket_pack, in one packing launch: the
+ * bucket's segment table (one segment per replica and param, contiguous params
+ * merged, plus the padding) is written into a fixed table inside the library's
+ * device code, at most 8192 segments (384 KB, held on every GPU that loads the
+ * library until exit), by small kernels that carry up to 600 segments each in
+ * their launch parameters. Nothing is copied from host memory, so the call
+ * does not wait for the stream. A bigger bucket returns ZR_ERR_UNSUPPORTED.
+ * The first call on a device looks the table's address up
  * (cudaGetSymbolAddress); make that first call before any stream capture. All
  * calls share the table: calls on one stream are ordered, but calls whose work
  * overlaps on the GPU (different streams) race on it.

@@ -318,6 +318,18 @@ def allreduce_avg(world: int, bucket: Sequence[np.ndarray], scale: float, postsc
     return out
 
 
+def average(world: int, x: Sequence[np.ndarray], scale: float) -> np.ndarray:
+    """The averaged gradient of every position of x[0..world-1] (one array):
+    zro_allreduce_avg with postscale 1 and every replica's output the same
+    array, so a caller comparing long flat ranges holds one result, not N."""
+    n = int(x[0].shape[0])
+    code = _dtype_code(x[0])
+    out = np.empty(n, dtype=np.float32)
+    outs = (ctypes.c_void_p * world)(*([_ptr(out)] * world))
+    _check(lib().zro_allreduce_avg(world, n, _ptr_array(x), code, scale, 1.0, outs), "zro_allreduce_avg")
+    return out
+
+
 def f16_to_f32(h: np.ndarray) -> np.ndarray:
     h = np.ascontiguousarray(h, dtype=np.float16)
     out = np.empty(h.shape, dtype=np.float32)

@@ -96,3 +96,27 @@ def test_pointer_tables_survive_until_the_call(monkeypatch):
     zr.zr_bucket_pack(lay, 0, grads, T["x"], stream=s)
     assert fake.calls["pack"]["grads"] == [0x7000000 + 0x100 * j for j in range(2 * world)]
     assert fake.calls["pack"]["out"] == base["x"]
+
+
+def test_pointer_array_from_a_generator_keeps_every_tensor():
+    """A PtrArray built from a generator addresses and keeps the same objects:
+    tensors made inside the generator stay alive as long as the array."""
+    import weakref
+    from zero_partition_aware_gb300 import build
+    build.build()
+    from zero_partition_aware_gb300 import zr
+    made = []
+
+    def gen():
+        for i in range(5):
+            t = FakeTensor(0x9000000 + 0x100 * i)
+            made.append(weakref.ref(t))
+            yield t
+
+    arr = zr.PtrArray(gen())
+    gc.collect()
+    assert [int(a) for a in arr.array] == [0x9000000 + 0x100 * i for i in range(5)]
+    assert all(r() is not None for r in made)
+    del arr
+    gc.collect()
+    assert all(r() is None for r in made)

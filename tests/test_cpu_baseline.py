@@ -49,3 +49,13 @@ def test_traffic_hash_ignores_comments_not_code():
     c = "int f(int x) {\n    return x + 2;\n}\n"
     assert bench.code_only(a) == bench.code_only(b) != bench.code_only(c)
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_traffic_hash_follows_the_compile_flags(monkeypatch):
+    """The profiled traffic is keyed to the host launch code and the nvcc flags
+    too: a changed flag must move the hash."""
+    bench = _bench()
+    from zero_partition_aware_gb300 import build as zb
+    h0 = bench.kernel_source_hash()
+    monkeypatch.setattr(zb, "COMMON_FLAGS", zb.COMMON_FLAGS + ["-DZR_SOMETHING"])
+    assert bench.kernel_source_hash() != h0

@@ -1,15 +1,20 @@
-"""The step with gradients arriving from host memory, pipelined per bucket (GPU).
+"""The pipelined and overlapped steps (GPU) against the oracle.
 
 DPGroup.step_direct_from_host copies each bucket's gradients in on one
 stream, runs zr_step_direct on another and copies the bucket's bf16 params out
-on a third. Its results must be bit-identical to the same step with the
-gradients already on the device, and the host copy of the parameter buffer
-must equal the device's.
+on a third. DPGroup.step_overlapped packs bucket b+1 on a second stream while
+bucket b is reduced ("DeepSpeed ZeRO 通信优化深度解析" §四, §五 overlap_comm;
+"Megatron-LM 分布式训练（四）" §"梯度缓冲区+分桶+overlap"). A stream-ordering
+mistake would corrupt the overlapped path and the sequential one alike, so
+both are held to the oracle's bucket path (bucket_pack, then rs_adam_fused
+per bucket, in bucket order), bit for bit, over two consecutive steps where
+the pipeline reuses its buffers.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from zero_partition_aware_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -27,6 +32,28 @@ def mods():
 
 def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32).numpy()
+
+
+def _oracle_steps(numel, world, B, grads_flat, master, m, v, hp, steps, arrival=None):
+    """`steps` oracle steps from the flat [T] state and each rank's flat [T] bf16
+    gradients: per bucket, in bucket order, the pack and the fused step.
+    Returns the partitions (master, m, v as [world][S] fp32) and the bf16 params."""
+    lay = oracle.layout(numel, world, B, order=arrival)
+    g = [oracle.params_from_flat(lay, W.bf16_bits(t.cpu())) for t in grads_flat]
+    p, mm, vv = (oracle.shards_from_flat(lay, t.cpu().numpy()) for t in (master, m, v))
+    param = np.zeros(lay.P, np.uint16)
+    scale = float(np.float32(1.0 / world))
+    for _ in range(steps):
+        for b in range(lay.n_buckets):
+            oracle.rs_adam_fused(lay, b, oracle.bucket_pack(lay, b, g), scale, p, mm, vv, hp, param)
+    return lay, p, mm, vv, param
+
+
+def _assert_oracle(grp, lay, p, m, v, param, what):
+    assert np.array_equal(_bits(grp.param[: lay.P]).view(np.uint16), param), f"{what}: params"
+    for r in range(lay.world):
+        for dev, ref, nm in ((grp.master[r], p[r], "master"), (grp.m[r], m[r], "m"), (grp.v[r], v[r], "v")):
+            assert np.array_equal(_bits(dev).view(np.uint32), ref.view(np.uint32)), f"{what}: {nm} of rank {r}"
 
 
 @pytest.mark.parametrize("world,n,hi,B", [(4, 40, 30_000, 60_000), (16, 120, 200_000, 1 << 21)])
@@ -52,7 +79,8 @@ def test_from_host_equals_device_resident(mods, world, n, hi, B):
 
     # reference: gradients resident on the device
     ref, ref_plan = group(arenas)
-    ref.step_direct(ref_plan, hp)
+    for _ in range(2):
+        ref.step_direct(ref_plan, hp)
     # the pipelined step: device arenas start as garbage, the host holds the gradients
     dev = [torch.full_like(a, float("nan")) for a in arenas]
     host = [a.cpu().pin_memory() for a in arenas]
@@ -65,8 +93,17 @@ def test_from_host_equals_device_resident(mods, world, n, hi, B):
         hiw[b] = offs[i] + k
     pairs = [[(h[lo[b]:hiw[b]], d[lo[b]:hiw[b]]) for h, d in zip(host, dev)] for b in range(L.n_buckets)]
     param_host = torch.full((L.P,), -1, dtype=torch.int16).pin_memory().view(torch.bfloat16)
-    got.step_direct_from_host(got_plan, hp, pairs, param_host)
+    for step in range(2):  # the second step reuses the device arenas and the host buffer
+        if step:
+            for d in dev:
+                d.fill_(float("nan"))
+            param_host.view(torch.int16).fill_(-1)
+        got.step_direct_from_host(got_plan, hp, pairs, param_host)
     torch.cuda.synchronize()
+    flat = [torch.cat([a[o:o + k] for o, k in zip(offs, numel)]) for a in arenas]
+    lay, p, m_, v_, param = _oracle_steps(numel, world, B, flat, master, m, v, hp, 2)
+    _assert_oracle(got, lay, p, m_, v_, param, "host-pipelined step")
+    assert np.array_equal(_bits(param_host).view(np.uint16), param), "the host copy of the params"
     assert np.array_equal(_bits(got.param[: L.P]), _bits(ref.param[: L.P]))
     assert np.array_equal(_bits(param_host), _bits(ref.param[: L.P]))
     for r in range(world):
@@ -76,11 +113,12 @@ def test_from_host_equals_device_resident(mods, world, n, hi, B):
 
 @pytest.mark.parametrize("flat_order", [False, True], ids=["fused", "flat_order_reverse_arrival"])
 @pytest.mark.parametrize("world,n,hi,B", [(4, 40, 30_000, 60_000), (16, 120, 200_000, 1 << 21), (8, 5, 1000, 1)])
-def test_overlapped_pack_and_fused_equal_the_sequential_step(mods, world, n, hi, B, flat_order):
+def test_overlapped_pack_and_fused_equal_the_oracle(mods, world, n, hi, B, flat_order):
     """Packing bucket b+1 on a second stream while bucket b is reduced (two
-    bucket buffer sets) gives the sequential step's results bit for bit; with
-    flat_order, under backward arrival, each bucket is reduced by the direct
-    kernel over the buffer set's param slices."""
+    bucket buffer sets), two steps in a row, equals the oracle's two steps bit
+    for bit, and so does the sequential step; with flat_order, under backward
+    arrival, each bucket is reduced by the direct kernel over the buffer set's
+    param slices."""
     engine, zr = mods
     rng = np.random.default_rng(100 + world)
     numel = W.random_numels(rng, n, 1, hi)
@@ -104,6 +142,10 @@ def test_overlapped_pack_and_fused_equal_the_sequential_step(mods, world, n, hi,
         b.step_overlapped(plans, hp, flat_order=flat_order)
     a.step(ta, hp, plan=a.pack_plan(ta))
     torch.cuda.synchronize()
+    lay, p, m_, v_, param = _oracle_steps(numel, world, B, [inp["grads"][k][0] for k in range(world)],
+                                          inp["master"], inp["m"], inp["v"], hp, 2, arrival=arrival)
+    _assert_oracle(b, lay, p, m_, v_, param, "overlapped step")
+    _assert_oracle(a, lay, p, m_, v_, param, "sequential step")
     assert np.array_equal(_bits(a.param[: L.P]), _bits(b.param[: L.P]))
     for r in range(world):
         for x, y in ((a.master[r], b.master[r]), (a.m[r], b.m[r]), (a.v[r], b.v[r])):

@@ -122,65 +122,3 @@ def test_fused_acc_rejects(zr):
     with pytest.raises(zr.ZrError) as e:
         zr.zr_rs_adam_fused_acc(lay, 0, two, [t.to(torch.bfloat16) for t in two], 0.5, two, two, two, W.AdamW())
     assert e.value.status == zr.ZR_ERR_UNSUPPORTED
-
-
-def test_full_size_llama_micro_steps_folded(zr):
-    """Llama 1.1B at full size, world 8, 4 bf16 micro-steps: the first started by
-    zr_grad_accumulate_first, the next two added, the last folded into the fused
-    step, as the benchmark runs it; checked at sampled positions."""
-    from zero_partition_aware_gb300.engine import DPGroup
-    wl = W.WORKLOADS["llama_1p1b"]
-    lay = oracle.layout(list(wl.numel), wl.world, wl.bucket)
-    rng = np.random.default_rng(2)
-    f = np.unique(np.concatenate([rng.integers(0, lay.P, 20000), np.arange(lay.T - 3, lay.P),
-                                  np.arange(lay.world) * lay.S]))
-    torch.cuda.empty_cache()
-    inp = W.draw_inputs(wl, "cuda", seed=0)
-    grp = DPGroup(list(wl.numel), wl.world, wl.bucket, grad_dtype=torch.float32, allocate_buckets=False)
-    grp.load_flat(inp["master"], inp["m"], inp["v"])
-    del inp["master"], inp["m"], inp["v"]
-    r_, j_ = f // lay.S, f % lay.S
-
-    def at(shards):
-        out = np.empty(len(f), np.float32)
-        for rr in np.unique(r_):
-            sel = r_ == rr
-            out[sel] = shards[rr][torch.from_numpy(j_[sel]).cuda()].cpu().numpy()
-        return out
-
-    p0, m0, v0 = at(grp.master), at(grp.m), at(grp.v)
-    real = f < lay.T
-    fr = torch.from_numpy(f[real]).cuda()
-    main = [torch.empty(lay.P, dtype=torch.float32, device="cuda") for _ in range(wl.world)]
-    lasts = []
-    mbs = np.zeros((wl.world, wl.micro_steps, len(f)), np.uint16)
-    for k in range(wl.world):
-        for s in range(wl.micro_steps):
-            g = inp["grads"][k][s]
-            mbs[k, s, real] = _bits(g[fr])
-            if s == 0:
-                zr.zr_grad_accumulate_first(main[k][: lay.T], g)
-            elif s < wl.micro_steps - 1:
-                zr.zr_grad_accumulate(main[k][: lay.T], g)
-            else:
-                last = torch.zeros(lay.P, dtype=torch.bfloat16, device="cuda")
-                last[: lay.T].copy_(g)
-                lasts.append(last)
-            inp["grads"][k][s] = None
-        main[k][lay.T:].zero_()
-    grp.step_in_place_acc(grp.main_grad_views(main), grp.main_grad_views(lasts), wl.adam)
-    torch.cuda.synchronize()
-    x = []
-    for k in range(wl.world):
-        acc = np.zeros(len(f), np.float32)
-        for s in range(wl.micro_steps):
-            oracle.grad_accumulate(acc, mbs[k, s])
-        x.append(acc)
-    avg = oracle.allreduce_avg(wl.world, x, grp.scale)[0]
-    p, m, v = p0.copy(), m0.copy(), v0.copy()
-    oracle.adamw(p, m, v, avg, wl.adam)
-    assert np.array_equal(at(grp.master).view(np.uint32), p.view(np.uint32))
-    assert np.array_equal(at(grp.m).view(np.uint32), m.view(np.uint32))
-    assert np.array_equal(at(grp.v).view(np.uint32), v.view(np.uint32))
-    want_param = np.where(real, oracle.f32_to_bf16(p), 0).astype(np.uint16)
-    assert np.array_equal(_bits(grp.param[torch.from_numpy(f).cuda()]), want_param)

@@ -5,8 +5,7 @@ every stream and several world sizes (including the >64 launch-parameter
 layout); outputs are compared bit-exactly, which is stricter than the
 required 1e-6 relative (fp32) and 2^-8 relative (bf16). Guard zones around
 every output check that nothing outside it is written. The full-size
-workloads run in the bench's launch configuration and are checked on
-sampled positions that the oracle computes one by one.
+workloads are compared at every element in tests/test_gpu_whole.py.
 """
 import numpy as np
 import pytest
@@ -565,106 +564,3 @@ def test_tiny_workload_end_to_end(zr):
         _assert_same(_bits(grp.m[r]), m[r], f"m {r}")
         _assert_same(_bits(grp.v[r]), v[r], f"v {r}")
     _assert_same(_bits(grp.param[: lay.P]), param, "param", dtype="bf16")
-
-
-def _sample_positions(lay, rng, k=20000):
-    f = list(rng.integers(0, lay.P, k))
-    for b in range(lay.n_buckets):  # every bucket edge and every partition edge
-        s, nb = lay.bucket(b)
-        f += [s, s + 1, s + nb - 1, s + nb - 2]
-    for r in range(lay.world):
-        f += [r * lay.S, r * lay.S + 1, (r + 1) * lay.S - 1]
-    f += list(range(max(lay.T - 3, 0), lay.P))  # the tail and its padding
-    f = np.unique(np.clip(np.array(f, dtype=np.int64), 0, lay.P - 1))
-    return f
-
-
-def _gather_flat(tensors_by_rank, lay, f):
-    """Values at flat positions f from per-rank shards (CPU numpy)."""
-    r = f // lay.S
-    j = f - r * lay.S
-    out = np.empty(len(f), np.float32)
-    for rr in np.unique(r):
-        sel = r == rr
-        idx = torch.from_numpy(j[sel]).cuda()
-        out[sel] = tensors_by_rank[rr][idx].cpu().numpy()
-    return out
-
-
-@pytest.mark.parametrize("name,direct", [("gpt2_124m", False), ("llama_1p1b", False), ("irregular_10k", False),
-                                         ("llama3_3b", False), ("irregular_10k", True), ("gpt2_124m", True)])
-def test_full_size_workload_sampled(zr, name, direct):
-    """Full-size workload, launched exactly as bench.py launches it, checked at sampled positions."""
-    from zero_partition_aware_gb300.engine import DPGroup
-    wl = W.WORKLOADS[name]
-    lay = oracle.layout(list(wl.numel), wl.world, wl.bucket)
-    rng = np.random.default_rng(0)
-    f = _sample_positions(lay, rng)
-    torch.cuda.empty_cache()
-    inp = W.draw_inputs(wl, "cuda", seed=0)
-    fp32_path = wl.micro_steps > 1
-    grp = DPGroup(list(wl.numel), wl.world, wl.bucket, grad_dtype=torch.float32 if fp32_path else torch.bfloat16,
-                  allocate_buckets=not (fp32_path or direct))
-    grp.load_flat(inp["master"], inp["m"], inp["v"])
-    del inp["master"], inp["m"], inp["v"]
-    p0 = _gather_flat(grp.master, lay, f)
-    m0 = _gather_flat(grp.m, lay, f)
-    v0 = _gather_flat(grp.v, lay, f)
-    real = f < lay.T
-    fr = torch.from_numpy(f[real]).cuda()
-    if fp32_path:
-        # Megatron-style: micro-steps accumulate into a flat fp32 [P] buffer per rank, read in place
-        main = [torch.zeros(lay.P, dtype=torch.float32, device="cuda") for _ in range(wl.world)]
-        mbs = np.zeros((wl.world, wl.micro_steps, len(f)), np.uint16)
-        for k in range(wl.world):
-            for s in range(wl.micro_steps):
-                g = inp["grads"][k][s]
-                mbs[k, s, real] = _bits(g[fr])
-                zr.zr_grad_accumulate(main[k][: lay.T], g)
-                inp["grads"][k][s] = None
-        grp.step_in_place(grp.main_grad_views(main), wl.adam)
-        x = []
-        for k in range(wl.world):
-            acc = np.zeros(len(f), np.float32)
-            for s in range(wl.micro_steps):
-                oracle.grad_accumulate(acc, mbs[k, s])
-            x.append(acc)
-    else:
-        # DeepSpeed-style: each param's grad is its own tensor (512-byte aligned starts in an
-        # arena, as separate allocations sit); packed into the rank's IPG bucket, then reduced
-        offs = W.arena_offsets(wl.numel, 256)
-        size = offs[-1] + wl.numel[-1]
-        x = []
-        rows = []
-        for k in range(wl.world):
-            arena = torch.empty(size, dtype=torch.bfloat16, device="cuda")
-            src = inp["grads"][k][0]
-            views = [arena[o:o + nnum] for o, nnum in zip(offs, wl.numel)]
-            # copy the flat draw into the arena param by param (setup only)
-            for i, vv in enumerate(views):
-                vv.copy_(src[lay.offset[i]: lay.offset[i] + wl.numel[i]])
-            xk = np.zeros(len(f), np.uint16)
-            xk[real] = _bits(src[fr])
-            x.append(xk)
-            inp["grads"][k][0] = None
-            rows.append((arena, views))
-        table = grp.grad_table([v for _, v in rows])
-        if direct:
-            grp.step_direct(grp.direct_plan(table), wl.adam)
-        else:
-            grp.step(table, wl.adam, plan=grp.pack_plan(table))
-    torch.cuda.synchronize()
-    # oracle, position by position
-    avg = oracle.allreduce_avg(wl.world, x, grp.scale)[0]
-    p, m, v = p0.copy(), m0.copy(), v0.copy()
-    oracle.adamw(p, m, v, avg, wl.adam)
-    want_param = np.where(real, oracle.f32_to_bf16(p), 0).astype(np.uint16)
-    _assert_same(_gather_flat(grp.master, lay, f).view(np.uint32), p, f"{name} master")
-    _assert_same(_gather_flat(grp.m, lay, f).view(np.uint32), m, f"{name} m")
-    _assert_same(_gather_flat(grp.v, lay, f).view(np.uint32), v, f"{name} v")
-    got_param = _bits(grp.param[torch.from_numpy(f).cuda()])
-    _assert_same(got_param, want_param, f"{name} param", dtype="bf16")
-    if name == "irregular_10k":
-        # integer grads: the averaged gradient is exact, so the update is pinned by the closed form
-        assert np.all(np.abs(avg * 16 - np.rint(avg * 16)) == 0)
-

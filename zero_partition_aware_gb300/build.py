@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libzr.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-COMMON = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC,-Wall", "-I", INCLUDE, "-I", CSRC]
+COMMON_FLAGS = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC,-Wall"]
+COMMON = COMMON_FLAGS + ["-I", INCLUDE, "-I", CSRC]
 
 SOURCES = ["kernels.cu", "layout.cpp"]
 HEADERS = [os.path.join(INCLUDE, "zr.h"), os.path.join(CSRC, "zr_internal.h"), os.path.join(CSRC, "zr_kernels.cuh")]

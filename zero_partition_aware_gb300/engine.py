@@ -76,6 +76,10 @@ class DPGroup:
     def flat(self, shards: Sequence[torch.Tensor]) -> torch.Tensor:
         return torch.cat(list(shards))[: self.layout.T]
 
+    def flat_state(self) -> List[torch.Tensor]:
+        """master, m and v as the flat [P] buffers whose views are the partitions."""
+        return [buf[: self.layout.P] for buf in self._flat_state]
+
     def grad_table(self, grads: Sequence[Sequence[torch.Tensor]]) -> zr.PtrArray:
         """Host array [world * n_params] of device pointers, built once per set of grads."""
         return zr.PtrArray([t for row in grads for t in row])
@@ -213,6 +217,7 @@ class DPGroup:
         if getattr(self, "_grad", None) is None:
             S = self.layout.S  # views of one flat buffer, like master, m and v
             buf = torch.zeros(max(self.layout.P, 1), dtype=torch.float32, device=self.device)
+            self._grad_flat = buf[: self.layout.P]
             self._grad = [buf[r * S:(r + 1) * S] for r in range(self.world)]
             self._p_grad = zr.PtrArray(self._grad)
             self.check = zr.GradCheck()

@@ -170,9 +170,11 @@ class PtrArray:
     """A host array of device pointers, built once and reusable across calls."""
 
     def __init__(self, items: Iterable):
+        if not isinstance(items, np.ndarray):
+            items = list(items)  # one pass: a generator's tensors must be both addressed and kept alive
         vals = [_addr(t) or 0 for t in items]
         self.array = np.asarray(vals, dtype=np.uint64)
-        self._keep = list(items) if not isinstance(items, np.ndarray) else None
+        self._keep = items if not isinstance(items, np.ndarray) else None
 
     @property
     def ptr(self) -> int:
