@@ -1,9 +1,13 @@
 #!/usr/bin/env python3
 """Benchmark: params/s through the partition-aware ZeRO step on one GB300.
 
-One step is the whole hot path for every bucket, in order: IPG packing of each
-emulated rank's per-parameter bf16 gradients into its bucket, then the fused
-reduce-scatter (1/N predivide) + AdamW + bf16 cast. Default workload: the
+One step is the whole hot path over every bucket in one pass, with no bucket
+buffer (zr_step_direct_range): each emulated rank's per-parameter bf16
+gradients are read where they lie, sliced by partition as the IPG bucket
+would hold them, reduce-scattered with the 1/N predivide, and AdamW and the
+bf16 cast run on each partition, consecutive buckets sharing launches. The
+same step with the bucket materialised (planned pack, then the fused
+reduce-scatter + AdamW + cast per bucket) is reported beside it. Default workload: the
 irregular layout (10,000 log-uniform params, 718,175,492 elements, 16 emulated
 ranks, 2^24-element buckets, integer-valued grads), each rank's gradients laid
 out as separately allocated tensors (512-byte aligned starts). Inputs are
@@ -444,54 +448,73 @@ def run_gpu(args, rank, nranks, local, dist):
                               "(DPGroup.reduce_packed); two bucket buffer sets, ordered by events"},
     }
 
-    # the unfused steps, one kernel each (reduce-scatter, AdamW over the partitions, the
-    # gather-cast) and the all-reduce reference path, per bucket after the planned pack
+    # the unfused steps, one kernel each: the reduce-scatter and the all-reduce reference path
+    # over every bucket of one contiguous gradient buffer per rank (the buckets back to back in
+    # bucket order, filled once by the pack), AdamW over the partitions and the gather-cast
     from zero_partition_aware_gb300 import zr as _zr
     grads = grp.grad_shards()
-    ar_out = [torch.empty(max(grp.max_bucket, 1), dtype=torch.float32, device=device) for _ in range(wl.world)]
+    starts = [0]
+    for b in range(nbk):
+        starts.append(starts[-1] + L.bucket(b)[1])
+    gbuf = [torch.empty(starts[-1], dtype=grp.grad_dtype, device=device) for _ in range(wl.world)]
+    for b in range(nbk):
+        _zr.zr_bucket_pack(L, b, table, [t[starts[b]:starts[b + 1]] for t in gbuf], dtype=grp.zr_dtype, stream=stream)
+    p_gbuf = _zr.PtrArray(gbuf)
+    ar_out = [torch.empty(starts[-1], dtype=torch.float32, device=device) for _ in range(wl.world)]
     p_ar = _zr.PtrArray(ar_out)
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def unfused_step(timed):
-        t = [0.0, 0.0, 0.0, 0.0]
-        for b in range(nbk):
-            pack(b)
-            e = [ev() for _ in range(4)]
-            e[0].record(stream)
-            _zr.zr_reduce_scatter_avg(L, b, grp._p_buckets, grp.scale, grp._p_grad, dtype=grp.zr_dtype, stream=stream)
-            e[1].record(stream)
-            _zr.zr_allreduce_avg(L, b, grp._p_buckets, grp.scale, p_ar, dtype=grp.zr_dtype, stream=stream)
-            e[2].record(stream)
-            timed.append(("rs", e[0], e[1]))
-            timed.append(("ar", e[1], e[2]))
-        e = [ev() for _ in range(3)]
+        e = [ev() for _ in range(5)]
         e[0].record(stream)
-        _zr.zr_adam_shard_step(L, -1, grp._p_master, grp._p_m, grp._p_v, grp._p_grad, hp, stream=stream)
+        _zr.zr_reduce_scatter_avg_range(L, 0, nbk, p_gbuf, grp.scale, grp._p_grad, dtype=grp.zr_dtype, stream=stream)
         e[1].record(stream)
-        _zr.zr_gather_cast_bf16(L, grp._p_master, grp.param, stream=stream)
+        _zr.zr_allreduce_avg_range(L, 0, nbk, p_gbuf, grp.scale, p_ar, dtype=grp.zr_dtype, stream=stream)
         e[2].record(stream)
-        timed.append(("adam", e[0], e[1]))
-        timed.append(("cast", e[1], e[2]))
+        _zr.zr_adam_shard_step(L, -1, grp._p_master, grp._p_m, grp._p_v, grp._p_grad, hp, stream=stream)
+        e[3].record(stream)
+        _zr.zr_gather_cast_bf16(L, grp._p_master, grp.param, stream=stream)
+        e[4].record(stream)
+        timed += [("rs", e[0], e[1]), ("ar", e[1], e[2]), ("adam", e[2], e[3]), ("cast", e[3], e[4])]
+
+    def per_bucket_rs(timed):  # the per-bucket calls over the same buffer, for comparison
+        for b in range(nbk):
+            x = [t[starts[b]:starts[b + 1]] for t in gbuf]
+            e = [ev() for _ in range(3)]
+            e[0].record(stream)
+            _zr.zr_reduce_scatter_avg(L, b, x, grp.scale, grp._p_grad, dtype=grp.zr_dtype, stream=stream)
+            e[1].record(stream)
+            _zr.zr_allreduce_avg(L, b, x, grp.scale, [t[starts[b]:starts[b + 1]] for t in ar_out],
+                                 dtype=grp.zr_dtype, stream=stream)
+            e[2].record(stream)
+            timed += [("rs_pb", e[0], e[1]), ("ar_pb", e[1], e[2])]
 
     for _ in range(W_):
         unfused_step([])
+        per_bucket_rs([])
     torch.cuda.synchronize()
     marks = []
     for _ in range(args.steps):
         unfused_step(marks)
+    for _ in range(args.steps):
+        per_bucket_rs(marks)
     torch.cuda.synchronize()
-    tsum = {k: 0.0 for k in ("rs", "ar", "adam", "cast")}
+    tsum = {k: 0.0 for k in ("rs", "ar", "adam", "cast", "rs_pb", "ar_pb")}
     for k, a, b_ in marks:
         tsum[k] += a.elapsed_time(b_)
-    un_bytes = {"rs": L.P * (2 * wl.world + 4), "ar": L.P * (2 * wl.world + 4 * wl.world),
-                "adam": L.P * 28, "cast": L.P * 6}
     unfused = {}
     for k, name, bpp in (("rs", "reduce_scatter_avg", 2 * wl.world + 4), ("adam", "adam_shard_step", 28),
-                         ("cast", "gather_cast_bf16", 6), ("ar", "allreduce_avg", 6 * wl.world)):
-        g_ = gbs(un_bytes[k], tsum[k])
+                         ("cast", "gather_cast_bf16", 6), ("ar", "allreduce_avg", 6 * wl.world),
+                         ("rs_pb", "reduce_scatter_avg_per_bucket", 2 * wl.world + 4),
+                         ("ar_pb", "allreduce_avg_per_bucket", 6 * wl.world)):
+        g_ = gbs(L.P * bpp, tsum[k])
         unfused[name] = {"ms_per_step": round(tsum[k] / args.steps, 4), "GB_per_s": round(g_, 1),
                          "frac_of_peak": round(g_ / peak, 4), "bytes_per_param": bpp}
-    del ar_out, p_ar
+    unfused["how"] = ("reduce_scatter_avg and allreduce_avg: the grouped calls (zr_reduce_scatter_avg_range, "
+                      "zr_allreduce_avg_range) over one contiguous buffer per rank holding every bucket; "
+                      "*_per_bucket: one zr_reduce_scatter_avg / zr_allreduce_avg call per bucket of the same buffer")
+    del ar_out, p_ar, gbuf, p_gbuf
+    torch.cuda.empty_cache()
 
     clipped = None
     if not args.no_clipped:

@@ -134,7 +134,13 @@ const char *zr_status_string(int status);
 int zr_last_error(char *buf, size_t cap);
 int zr_version(void);
 /* Number of kernels this process has launched through libzr so far (all
- * threads, all devices); lets a caller count the launches of a region. */
+ * threads, all devices); lets a caller count the launches of a region.
+ * Failure injection for testing a caller's error handling: while the
+ * environment variable ZR_FAIL_AT_LAUNCH holds n >= 1, every kernel launch
+ * attempted once this count has reached n - 1 fails with ZR_ERR_CUDA (message
+ * "injected failure ...") before anything is enqueued; the entry point returns
+ * at that launch, so later launches of the same call are not made. The
+ * variable is read at every attempt; unset or 0, it has no effect. */
 int64_t zr_launch_count(void);
 
 /* ---- layout (host only) ------------------------------------------------ */
@@ -192,6 +198,15 @@ int zr_layout_runs(const zr_layout *layout, zr_run *out, int64_t cap, int64_t *n
 int zr_layout_bucket(const zr_layout *layout, int64_t b, int64_t *flat_start, int64_t *numel);
 /* Flat offset o_i of param i and the bucket it belongs to. */
 int zr_layout_param(const zr_layout *layout, int64_t param, int64_t *flat_offset, int64_t *bucket);
+/* Where each param's gradient starts inside its bucket, the offset at which
+ * zr_bucket_pack places it ([DS] §四: grads copied into the IPG bucket as they
+ * arrive): o_i minus the bucket's flat start under the flat arrival order,
+ * else the elements of the params that arrived before it into the same
+ * bucket. Writes min(cap, n_params) entries to out (may be NULL to query the
+ * count) and n_params to *n_out. A caller that reads packed buckets per param
+ * (for instance a zr_direct_plan over the bucket buffers' param slices)
+ * points into them with these offsets. */
+int zr_layout_bucket_positions(const zr_layout *layout, int64_t *out, int64_t cap, int64_t *n_out);
 
 /* ---- device steps ------------------------------------------------------ */
 
@@ -279,6 +294,25 @@ int zr_grad_accumulate_first(float *main_grad, const void *g, zr_dtype g_dtype, 
  */
 int zr_reduce_scatter_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
                           zr_dtype dtype, float scale, float *const *shard_grad, zr_stream stream);
+
+/*
+ * zr_reduce_scatter_avg for the buckets [bucket_first, bucket_first +
+ * bucket_count) of one contiguous gradient buffer per rank ([DS] §五
+ * contiguous_gradients: the gradients are copied into one contiguous buffer;
+ * [MG] §"梯度缓冲区+分桶+overlap": the flat gradient buffer is cut into buckets
+ * that are reduce-scattered in turn). grad_buf[k]: host array [world] of device
+ * pointers; rank k's buffer holds every bucket back to back in bucket order,
+ * bucket b at element offset numel_0 + ... + numel_{b-1} (in the flat arrival
+ * order that is the flat layout itself, padding last: the [P] gradient buffer);
+ * only the range's buckets are read. Consecutive buckets share launches up to
+ * 2^26 elements, and the results equal one zr_reduce_scatter_avg call per
+ * bucket (bucket_in[k] = grad_buf[k] + that offset), bit for bit.
+ * Differs from the per-bucket call only in where the buckets sit: one buffer
+ * per rank for the whole range instead of one bucket buffer per call.
+ */
+int zr_reduce_scatter_avg_range(const zr_layout *layout, int64_t bucket_first, int64_t bucket_count,
+                                const void *const *grad_buf, zr_dtype dtype, float scale,
+                                float *const *shard_grad, zr_stream stream);
 
 /*
  * AdamW over whole partitions ([MG] §"通信模式": each card updates its own
@@ -403,6 +437,18 @@ int zr_step_direct_range(const zr_direct_plan *plan, int64_t bucket_first, int64
  */
 int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
                      zr_dtype dtype, float scale, float postscale, float *const *out, zr_stream stream);
+
+/*
+ * zr_allreduce_avg over the buckets [bucket_first, bucket_first + bucket_count)
+ * of one contiguous gradient buffer per rank, laid out as for
+ * zr_reduce_scatter_avg_range; out[k] (host array [world] of device pointers,
+ * fp32) receives the same bucket-order layout, and only the range's positions
+ * are written. Consecutive buckets share launches up to 2^26 elements; the
+ * results equal one zr_allreduce_avg call per bucket, bit for bit.
+ */
+int zr_allreduce_avg_range(const zr_layout *layout, int64_t bucket_first, int64_t bucket_count,
+                           const void *const *grad_buf, zr_dtype dtype, float scale, float postscale,
+                           float *const *out, zr_stream stream);
 
 /* ---- global gradient check before the step -------------------------------- */
 

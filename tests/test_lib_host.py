@@ -277,21 +277,52 @@ def test_range_folded_and_first_validate_before_launch(zr):
 
 
 @pytest.mark.parametrize("kind", ["flat", "reverse", "random"])
-def test_param_bucket_offsets_match_the_oracle(zr, kind):
-    """The offsets the flat-order reduction of packed buckets points into: each
-    param's first element inside its bucket, as the oracle's layout places it
-    (the flat offset minus the bucket's flat start, or its bucket position)."""
-    from zero_partition_aware_gb300.engine import param_bucket_offsets
+def test_bucket_positions_match_the_oracle(zr, kind):
+    """zr_layout_bucket_positions: each param's first element inside its bucket,
+    as the oracle's layout places it (the flat offset minus the bucket's flat
+    start, or its bucket position)."""
     rng = np.random.default_rng(sum(map(ord, kind)))
     numel = W.random_numels(rng, 300, 1, 50_000)
     n = len(numel)
     order = None if kind == "flat" else (list(range(n - 1, -1, -1)) if kind == "reverse"
                                          else [int(x) for x in rng.permutation(n)])
     for world, B in ((8, 200_000), (16, 1), (3, 1 << 22)):
-        got = param_bucket_offsets(zr.Layout(numel, world, B, arrival=order))
+        got = zr.Layout(numel, world, B, arrival=order).bucket_positions()
         lay = oracle.layout(numel, world, B, order=order)
         if order is None:
             want = lay.offset - lay.bucket_range[lay.bucket_of, 0]
         else:
             want = lay.bucket_pos
         assert np.array_equal(got, want), (world, B)
+    L = zr._lib
+    lay = zr.Layout(numel, 4, 1000)
+    cnt = ctypes.c_int64()
+    assert L.zr_layout_bucket_positions(lay.handle, None, 0, ctypes.byref(cnt)) == zr.ZR_OK and cnt.value == n
+    assert L.zr_layout_bucket_positions(None, None, 0, ctypes.byref(cnt)) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_layout_bucket_positions(lay.handle, None, -1, ctypes.byref(cnt)) == zr.ZR_ERR_INVALID_ARG
+
+
+def test_grouped_calls_validate_before_launch(zr):
+    """zr_reduce_scatter_avg_range and zr_allreduce_avg_range reject bad ranges,
+    pointers and scales on the host."""
+    lay = zr.Layout([100, 200, 300], 2, 250)
+    L = zr._lib
+    two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    odd = (ctypes.c_void_p * 2)(0x1001, 0x2000)
+    nb = lay.n_buckets
+    for first, count in ((-1, 1), (0, nb + 1), (1, -1)):
+        assert L.zr_reduce_scatter_avg_range(lay.handle, first, count, two, zr.ZR_BF16, 0.5, two,
+                                             None) == zr.ZR_ERR_INVALID_ARG
+        assert L.zr_allreduce_avg_range(lay.handle, first, count, two, zr.ZR_BF16, 0.5, 1.0, two,
+                                        None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_reduce_scatter_avg_range(lay.handle, 0, 1, odd, zr.ZR_BF16, 0.5, two, None) == zr.ZR_ERR_ALIGN
+    assert L.zr_reduce_scatter_avg_range(lay.handle, 0, 1, two, zr.ZR_BF16, float("nan"), two,
+                                         None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_reduce_scatter_avg_range(lay.handle, 0, 1, two, zr.ZR_BF16, 0.5, None, None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_allreduce_avg_range(lay.handle, 0, 1, two, zr.ZR_BF16, 0.5, float("inf"), two,
+                                    None) == zr.ZR_ERR_INVALID_ARG
+    assert L.zr_allreduce_avg_range(lay.handle, 0, 1, two, zr.ZR_FP32, 0.5, 1.0, odd, None) == zr.ZR_ERR_ALIGN
+    assert L.zr_allreduce_avg_range(None, 0, 1, two, zr.ZR_BF16, 0.5, 1.0, two, None) == zr.ZR_ERR_INVALID_ARG
+    # an empty range is valid and launches nothing
+    assert L.zr_reduce_scatter_avg_range(lay.handle, 1, 0, two, zr.ZR_BF16, 0.5, two, None) == zr.ZR_OK
+    assert L.zr_allreduce_avg_range(lay.handle, 1, 0, two, zr.ZR_BF16, 0.5, 1.0, two, None) == zr.ZR_OK

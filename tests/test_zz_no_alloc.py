@@ -51,10 +51,10 @@ def test_noalloc_pack_equals_the_oracle_on_two_calls(zr, scattered, dtype):
     rng = np.random.default_rng((11 if scattered else 12) + (0 if dtype == "bf16" else 100))
     world = 8
     numel = W.random_numels(rng, 60, 1, 40_000)
-    B = 150_000
+    B = 60_000
     lay = zr.Layout(numel, world, B)
     olay = oracle.layout(numel, world, B)
-    assert lay.n_buckets >= 3
+    assert lay.n_buckets >= 2
     tdt, code, es = (torch.bfloat16, zr.ZR_BF16, 2) if dtype == "bf16" else (torch.float32, zr.ZR_FP32, 4)
     # gradients: each param its own tensor at a random element phase, or one flat tensor per rank
     keep, grads, host = [], [], []

@@ -318,6 +318,17 @@ int zr_layout_param(const zr_layout *L, int64_t param, int64_t *flat_offset, int
     return ZR_OK;
 }
 
+int zr_layout_bucket_positions(const zr_layout *L, int64_t *out, int64_t cap, int64_t *n_out) {
+    zr::clear_error();
+    if (!L) return fail(ZR_ERR_INVALID_ARG, "NULL layout");
+    if (cap < 0) return fail(ZR_ERR_INVALID_ARG, "cap < 0");
+    const int64_t n = L->n_params();
+    if (out)
+        for (int64_t i = 0; i < n && i < cap; ++i) out[i] = L->bucket_pos[i];
+    if (n_out) *n_out = n;
+    return ZR_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Accounting
 // ---------------------------------------------------------------------------

@@ -14,19 +14,9 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence
 
-import numpy as np
 import torch
 
 from . import zr
-
-
-def param_bucket_offsets(layout: zr.Layout) -> np.ndarray:
-    """[n_params]: where each param's first element sits inside its bucket (any
-    slice's bucket offset minus its offset in the param)."""
-    sl = layout.slices()
-    out = np.zeros(layout.n_params, np.int64)
-    out[sl[:, 0]] = sl[:, 4] - sl[:, 3]
-    return out
 
 
 class DPGroup:
@@ -123,7 +113,7 @@ class DPGroup:
             if not bufs:
                 raise ValueError(f"the group has no bucket buffer set {buffer_set}")
             L = self.layout
-            boff = param_bucket_offsets(L)
+            boff = L.bucket_positions()
             es = bufs[0].element_size()
             addrs = [int(buf.data_ptr()) + int(o) * es for buf in bufs for o in boff]
             plans[buffer_set] = zr.DirectPlan(L, zr.PtrArray(addrs), dtype=self.zr_dtype)

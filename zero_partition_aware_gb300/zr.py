@@ -94,6 +94,7 @@ _SIGS = {
     "zr_layout_runs": (ctypes.c_int, [_vp, _vp, _i64, _P(_i64)]),
     "zr_layout_bucket": (ctypes.c_int, [_vp, _i64, _P(_i64), _P(_i64)]),
     "zr_layout_param": (ctypes.c_int, [_vp, _i64, _P(_i64), _P(_i64)]),
+    "zr_layout_bucket_positions": (ctypes.c_int, [_vp, _vp, _i64, _P(_i64)]),
     "zr_bucket_pack": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
     "zr_pack_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _P(_vp)]),
     "zr_pack_plan_destroy": (ctypes.c_int, [_vp]),
@@ -102,6 +103,7 @@ _SIGS = {
     "zr_grad_accumulate": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_grad_accumulate_first": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_reduce_scatter_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
+    "zr_reduce_scatter_avg_range": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
     "zr_adam_shard_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _P(zr_adamw), _vp]),
     "zr_gather_cast_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "zr_rs_adam_fused": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp, _vp,
@@ -109,6 +111,7 @@ _SIGS = {
     "zr_rs_adam_fused_acc": (ctypes.c_int, [_vp, _i64, _vp, _vp, ctypes.c_int, _f32, _vp, _vp, _vp,
                                             _P(zr_adamw), _vp, _vp, _vp]),
     "zr_allreduce_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _f32, _vp, _vp]),
+    "zr_allreduce_avg_range": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _f32, _f32, _vp, _vp]),
     "zr_direct_plan_create": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _P(_vp)]),
     "zr_direct_plan_destroy": (ctypes.c_int, [_vp]),
     "zr_step_direct": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
@@ -321,6 +324,14 @@ class Layout:
         return np.array([[r.bucket, r.dst, r.bucket_offset, r.partition_offset, r.numel]
                          for r in buf[: n.value]], dtype=np.int64).reshape(-1, 5)
 
+    def bucket_positions(self) -> np.ndarray:
+        """[n_params]: where each param's gradient starts inside its bucket."""
+        out = np.zeros(max(self.n_params, 1), np.int64)
+        n = ctypes.c_int64()
+        _check(_lib.zr_layout_bucket_positions(self._h, out.ctypes.data, out.size, ctypes.byref(n)),
+               "zr_layout_bucket_positions")
+        return out[: n.value]
+
     def offsets(self) -> np.ndarray:
         return np.array([self.param(i)[0] for i in range(self.n_params)], dtype=np.int64)
 
@@ -432,6 +443,15 @@ def zr_reduce_scatter_avg(layout: Layout, bucket: int, bucket_in, scale: float, 
                                       _stream(stream)), "zr_reduce_scatter_avg")
 
 
+def zr_reduce_scatter_avg_range(layout: Layout, bucket_first: int, bucket_count: int, grad_buf, scale: float,
+                                shard_grad, dtype=None, stream=None) -> None:
+    """grad_buf: [world] buffers holding the buckets back to back in bucket order."""
+    d = _dtype_of(grad_buf, dtype)
+    x, g = _ptrs(grad_buf), _ptrs(shard_grad)
+    _check(_lib.zr_reduce_scatter_avg_range(layout.handle, int(bucket_first), int(bucket_count), x.ptr, d,
+                                            float(scale), g.ptr, _stream(stream)), "zr_reduce_scatter_avg_range")
+
+
 def zr_adam_shard_step(layout: Layout, rank: int, master, m, v, grad, hp, stream=None) -> None:
     h = _hp(hp)
     # the host pointer tables must outlive the call: keep them in locals
@@ -529,6 +549,14 @@ def zr_allreduce_avg(layout: Layout, bucket: int, bucket_in, scale: float, out, 
     px, po = _ptrs(bucket_in), _ptrs(out)
     _check(_lib.zr_allreduce_avg(layout.handle, int(bucket), px.ptr, d, float(scale), float(postscale), po.ptr,
                                  _stream(stream)), "zr_allreduce_avg")
+
+
+def zr_allreduce_avg_range(layout: Layout, bucket_first: int, bucket_count: int, grad_buf, scale: float, out,
+                           dtype=None, stream=None, postscale: float = 1.0) -> None:
+    d = _dtype_of(grad_buf, dtype)
+    px, po = _ptrs(grad_buf), _ptrs(out)
+    _check(_lib.zr_allreduce_avg_range(layout.handle, int(bucket_first), int(bucket_count), px.ptr, d, float(scale),
+                                       float(postscale), po.ptr, _stream(stream)), "zr_allreduce_avg_range")
 
 
 class GradCheck:
