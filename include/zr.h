@@ -219,6 +219,9 @@ int zr_layout_bucket_positions(const zr_layout *layout, int64_t *out, int64_t ca
  * bucket_out: host array [world] of device pointers, each receiving numel_b
  *   elements: param i's element e at offset o_i - bucket_start + e, and zeros
  *   at positions past T (the padding of the last bucket).
+ * The bucket is one buffer per emulated rank (each rank owns separate memory)
+ * rather than one [world][numel_b] buffer; a caller holding one such buffer
+ * passes the addresses of its rows.
  */
 int zr_bucket_pack(const zr_layout *layout, int64_t bucket, const void *const *grads,
                    zr_dtype dtype, void *const *bucket_out, zr_stream stream);
@@ -291,6 +294,8 @@ int zr_grad_accumulate_first(float *main_grad, const void *g, zr_dtype g_dtype, 
  * shard_grad: host array [world] of device pointers, S fp32 each; only the
  *   entries of ranks the bucket intersects are read, only positions inside
  *   the bucket are written.
+ * bucket_in is a host array of one buffer per rank rather than one
+ * [world][numel_b] buffer (pass its rows' addresses to use one).
  */
 int zr_reduce_scatter_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
                           zr_dtype dtype, float scale, float *const *shard_grad, zr_stream stream);
@@ -434,6 +439,9 @@ int zr_step_direct_range(const zr_direct_plan *plan, int64_t bucket_first, int64
  * means postscale = 1, which leaves the average unchanged bit for bit.
  * out: host array [world] of device pointers, numel_b fp32 each.
  * ZR_ERR_INVALID_ARG if postscale is not finite.
+ * bucket_in and out are host arrays of one buffer per rank rather than one
+ * [world][numel_b] buffer each, and postscale is an argument of its own
+ * (1.0f for the plain average).
  */
 int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const *bucket_in,
                      zr_dtype dtype, float scale, float postscale, float *const *out, zr_stream stream);
