@@ -400,8 +400,12 @@ int zr_rs_adam_fused_acc(const zr_layout *layout, int64_t bucket, const float *c
  * grad_start_offset; [DS] §四). One kernel launch per bucket and per 256
  * runs of it (plus one per further 1,024 tiles that cross a param boundary,
  * when a launch has more).
- * The plan is not modified by zr_step_direct: calls for different buckets
- * may run on different streams. world <= 32 (ZR_ERR_UNSUPPORTED above).
+ * The plan also holds, per bucket, 32 bytes of counters: the warps of a
+ * launch that starts at that bucket take their tiles from them as they go
+ * (SMs that run faster take more), and the launch leaves them at zero. Calls whose
+ * buckets are disjoint may therefore run on different streams at once; calls
+ * that share a bucket must be ordered (they write the same elements anyway).
+ * world <= 32 (ZR_ERR_UNSUPPORTED above).
  * master, m, v, shard_grad_out, param_bf16: as for zr_rs_adam_fused.
  */
 typedef struct zr_direct_plan zr_direct_plan;
