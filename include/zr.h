@@ -586,6 +586,24 @@ int zr_gradcheck_read(const zr_gradcheck *chk, zr_stream stream, zr_grad_stats *
 int zr_arith_check(int32_t which, uint64_t begin, uint64_t count, const zr_adamw *hp,
                    uint64_t *mismatches, uint64_t *bad, int32_t n_bad);
 
+/* ---- bounds-checked build ------------------------------------------------ */
+
+/*
+ * The library also builds as libzr_checked.so (compiled with ZR_CHECKED),
+ * with the same entry points. There, every range a kernel takes from its
+ * launch's plan for its vector accesses is checked before the access (a tile
+ * inside its run, a replica's tile inside its param's gradient, a packing
+ * super-tile inside its segment, a listed element's param inside the
+ * bucket); a failed check skips that access or takes the element-by-element
+ * path instead, and is counted on the device. The pages have no counterpart:
+ * it is a check of this library's planning, for tests (no GPU has to fault).
+ * zr_debug_checks waits for the device, then gives the number of failed
+ * checks since the last reset, the first one's check code and element, and
+ * with reset != 0 clears them. Any pointer may be NULL. In the ordinary
+ * build it returns ZR_ERR_UNSUPPORTED.
+ */
+int zr_debug_checks(int32_t reset, uint64_t *count, int32_t *first_code, int64_t *first_where);
+
 /* ---- accounting (host only) -------------------------------------------- */
 
 /* The AdamW scalars the kernels use for `hp` (see zr_adamw_scalars). */

@@ -326,3 +326,18 @@ def test_grouped_calls_validate_before_launch(zr):
     # an empty range is valid and launches nothing
     assert L.zr_reduce_scatter_avg_range(lay.handle, 1, 0, two, zr.ZR_BF16, 0.5, two, None) == zr.ZR_OK
     assert L.zr_allreduce_avg_range(lay.handle, 1, 0, two, zr.ZR_BF16, 0.5, 1.0, two, None) == zr.ZR_OK
+
+
+def test_bounds_checked_build_exports_the_same_calls(zr):
+    """libzr_checked.so exports every declared call too; only it answers
+    zr_debug_checks (the ordinary build refuses with ZR_ERR_UNSUPPORTED)."""
+    from zero_partition_aware_gb300 import build
+    chk = ctypes.CDLL(build.LIB_CHECKED)
+    for name in zr.EXPORTED:
+        assert hasattr(chk, name), name
+    n = ctypes.c_uint64()
+    assert zr._lib.zr_debug_checks(0, ctypes.byref(n), None, None) == zr.ZR_ERR_UNSUPPORTED
+    import torch
+    if not torch.cuda.is_available():  # the checked build reaches for the device
+        chk.zr_debug_checks.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        assert chk.zr_debug_checks(0, ctypes.byref(n), None, None) in (zr.ZR_ERR_CUDA, zr.ZR_ERR_STATE)

@@ -2,7 +2,8 @@
 
 Two translation units compiled in parallel by nvcc, linked with the static
 CUDA runtime; a linker version script exports only the ``zr_*`` entry points
-declared in ``include/zr.h``.
+declared in ``include/zr.h``. The same kernels compiled with ZR_CHECKED (the
+bounds-checked build, for tests) are linked into libzr_checked.so beside it.
 """
 from __future__ import annotations
 
@@ -18,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libzr.so")
+LIB_CHECKED = os.path.join(OUT_DIR, "libzr_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC,-Wall"]
 COMMON = COMMON_FLAGS + ["-I", INCLUDE, "-I", CSRC]
@@ -46,11 +48,14 @@ def _foreign(path: str) -> bool:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB) or _foreign(LIB):
-        return True
-    t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [__file__]
-    return any(os.path.getmtime(d) > t for d in deps)
+    for lib in (LIB, LIB_CHECKED):
+        if not os.path.exists(lib) or _foreign(lib):
+            return True
+        t = os.path.getmtime(lib)
+        if any(os.path.getmtime(d) > t for d in deps):
+            return True
+    return False
 
 
 def _run(cmd, verbose):
@@ -71,24 +76,29 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     os.makedirs(OUT_DIR, exist_ok=True)
     nv = nvcc()
     with tempfile.TemporaryDirectory(prefix="zr_build_") as tmp:
-        objs, cmds = [], []
+        objs = {LIB: [], LIB_CHECKED: []}
+        cmds = []
         for src in SOURCES:
-            obj = os.path.join(tmp, src + ".o")
-            cmd = [nv, *COMMON, "-c", os.path.join(CSRC, src), "-o", obj]
-            if src.endswith(".cu"):
-                cmd[1:1] = ARCH + ["-lineinfo"]
-                if ptxas_verbose:
-                    cmd.insert(1, "-Xptxas=-v")
-            objs.append(obj)
-            cmds.append(cmd)
+            variants = [(LIB, []), (LIB_CHECKED, ["-DZR_CHECKED"])] if src.endswith(".cu") else [(None, [])]
+            for lib, defs in variants:
+                obj = os.path.join(tmp, src + ("_checked" if defs else "") + ".o")
+                cmd = [nv, *COMMON, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
+                if src.endswith(".cu"):
+                    cmd[1:1] = ARCH + ["-lineinfo"]
+                    if ptxas_verbose and not defs:
+                        cmd.insert(1, "-Xptxas=-v")
+                for target in ([lib] if lib else [LIB, LIB_CHECKED]):
+                    objs[target].append(obj)
+                cmds.append(cmd)
         with ThreadPoolExecutor(len(cmds)) as ex:
             list(ex.map(lambda c: _run(c, verbose), cmds))
         vs = os.path.join(tmp, "exports.map")
         with open(vs, "w") as f:
             f.write("{ global: zr_*; local: *; };\n")
-        tmp_lib = LIB + f".{os.getpid()}.tmp"
-        _run([nv, *ARCH, "-shared", "-o", tmp_lib, *objs, "-Xlinker", f"--version-script={vs}"], verbose)
-        os.replace(tmp_lib, LIB)
+        for lib in (LIB, LIB_CHECKED):
+            tmp_lib = lib + f".{os.getpid()}.tmp"
+            _run([nv, *ARCH, "-shared", "-o", tmp_lib, *objs[lib], "-Xlinker", f"--version-script={vs}"], verbose)
+            os.replace(tmp_lib, lib)
     return LIB
 
 

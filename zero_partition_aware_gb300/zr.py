@@ -14,9 +14,11 @@ from typing import Iterable, Optional, Sequence, Union
 
 import numpy as np
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libzr.so")
+# ZR_LIB names another build of the library to load (the bounds-checked
+# libzr_checked.so, for tests); by default the in-tree libzr.so.
+_LIB_PATH = os.environ.get("ZR_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libzr.so")
 if not os.path.exists(_LIB_PATH):
-    raise ImportError(f"libzr.so is not built ({_LIB_PATH} missing); run zero_partition_aware_gb300.build.build()")
+    raise ImportError(f"libzr is not built ({_LIB_PATH} missing); run zero_partition_aware_gb300.build.build()")
 _lib = ctypes.CDLL(_LIB_PATH)
 
 ZR_OK = 0
@@ -126,6 +128,7 @@ _SIGS = {
     "zr_adam_clip_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _P(zr_adamw), _vp, _vp, _vp]),
     "zr_gradcheck_read": (ctypes.c_int, [_vp, _vp, _P(zr_grad_stats)]),
     "zr_adamw_prepare": (ctypes.c_int, [_P(zr_adamw), _P(zr_adamw_scalars)]),
+    "zr_debug_checks": (ctypes.c_int, [_i32, _P(ctypes.c_uint64), _P(_i32), _P(_i64)]),
     "zr_arith_check": (ctypes.c_int, [_i32, ctypes.c_uint64, ctypes.c_uint64, _P(zr_adamw),
                                       _P(ctypes.c_uint64), _P(ctypes.c_uint64), _i32]),
     "zr_comm_bytes": (ctypes.c_int, [_vp, _i32, _i32, _P(ctypes.c_double)]),
@@ -649,6 +652,15 @@ def zr_arith_check(which: int, begin: int, count: int, hp=None):
     _check(_lib.zr_arith_check(int(which), int(begin), int(count), ctypes.byref(h), ctypes.byref(n), bad, 8),
            "zr_arith_check")
     return n.value, list(bad[: min(n.value, 8)])
+
+
+def zr_debug_checks(reset: bool = False):
+    """(failed checks, first check code, first element) of the bounds-checked
+    build (ZrError ZR_ERR_UNSUPPORTED from the ordinary one)."""
+    n, code, where = ctypes.c_uint64(), ctypes.c_int32(), ctypes.c_int64()
+    _check(_lib.zr_debug_checks(int(bool(reset)), ctypes.byref(n), ctypes.byref(code), ctypes.byref(where)),
+           "zr_debug_checks")
+    return n.value, code.value, where.value
 
 
 def zr_adamw_prepare(hp) -> dict:
