@@ -456,11 +456,22 @@ def run_gpu(args, rank, nranks, local, dist):
     starts = [0]
     for b in range(nbk):
         starts.append(starts[-1] + L.bucket(b)[1])
-    gbuf = [torch.empty(starts[-1], dtype=grp.grad_dtype, device=device) for _ in range(wl.world)]
-    for b in range(nbk):
-        _zr.zr_bucket_pack(L, b, table, [t[starts[b]:starts[b + 1]] for t in gbuf], dtype=grp.zr_dtype, stream=stream)
+    torch.cuda.empty_cache()
+    free = torch.cuda.mem_get_info(torch.device(device))[0]
+    if wl.world * starts[-1] * (grp.buckets[0].element_size() if grp.buckets else 2) * 3 > 0.9 * free:
+        return_unfused = {"skipped": "the contiguous gradient buffers and the all-reduce outputs would not fit "
+                                     f"({wl.world} ranks x {starts[-1]} elements)"}
+    else:
+        return_unfused = None
+    gbuf = [torch.empty(starts[-1] if return_unfused is None else 1, dtype=grp.grad_dtype, device=device)
+            for _ in range(wl.world)]
+    if return_unfused is None:
+        for b in range(nbk):
+            _zr.zr_bucket_pack(L, b, table, [t[starts[b]:starts[b + 1]] for t in gbuf], dtype=grp.zr_dtype,
+                               stream=stream)
     p_gbuf = _zr.PtrArray(gbuf)
-    ar_out = [torch.empty(starts[-1], dtype=torch.float32, device=device) for _ in range(wl.world)]
+    ar_out = [torch.empty(starts[-1] if return_unfused is None else 1, dtype=torch.float32, device=device)
+              for _ in range(wl.world)]
     p_ar = _zr.PtrArray(ar_out)
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
@@ -489,27 +500,38 @@ def run_gpu(args, rank, nranks, local, dist):
             e[2].record(stream)
             timed += [("rs_pb", e[0], e[1]), ("ar_pb", e[1], e[2])]
 
-    for _ in range(W_):
-        unfused_step([])
-        per_bucket_rs([])
-    torch.cuda.synchronize()
     marks = []
-    for _ in range(args.steps):
-        unfused_step(marks)
-    for _ in range(args.steps):
-        per_bucket_rs(marks)
-    torch.cuda.synchronize()
-    tsum = {k: 0.0 for k in ("rs", "ar", "adam", "cast", "rs_pb", "ar_pb")}
-    for k, a, b_ in marks:
-        tsum[k] += a.elapsed_time(b_)
-    unfused = {}
-    for k, name, bpp in (("rs", "reduce_scatter_avg", 2 * wl.world + 4), ("adam", "adam_shard_step", 28),
-                         ("cast", "gather_cast_bf16", 6), ("ar", "allreduce_avg", 6 * wl.world),
-                         ("rs_pb", "reduce_scatter_avg_per_bucket", 2 * wl.world + 4),
-                         ("ar_pb", "allreduce_avg_per_bucket", 6 * wl.world)):
-        g_ = gbs(L.P * bpp, tsum[k])
-        unfused[name] = {"ms_per_step": round(tsum[k] / args.steps, 4), "GB_per_s": round(g_, 1),
-                         "frac_of_peak": round(g_ / peak, 4), "bytes_per_param": bpp}
+    if return_unfused is None:
+        for _ in range(W_):
+            unfused_step([])
+            per_bucket_rs([])
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            unfused_step(marks)
+        for _ in range(args.steps):
+            per_bucket_rs(marks)
+        torch.cuda.synchronize()
+    if return_unfused is None:
+        tsum = {k: 0.0 for k in ("rs", "ar", "adam", "cast", "rs_pb", "ar_pb")}
+        for k, a, b_ in marks:
+            tsum[k] += a.elapsed_time(b_)
+        unfused = {}
+        w16 = wl.world == 16
+        traffic_of = {"rs": ["reduce_scatter_range_bf16_w16"], "adam": ["adam_shard_w16"],
+                      "ar": ["allreduce_pass_bf16_w16", "allreduce_bcast_w16"]}
+        for k, name, bpp in (("rs", "reduce_scatter_avg", 2 * wl.world + 4), ("adam", "adam_shard_step", 28),
+                             ("cast", "gather_cast_bf16", 6), ("ar", "allreduce_avg", 6 * wl.world),
+                             ("rs_pb", "reduce_scatter_avg_per_bucket", 2 * wl.world + 4),
+                             ("ar_pb", "allreduce_avg_per_bucket", 6 * wl.world)):
+            g_ = gbs(L.P * bpp, tsum[k])
+            unfused[name] = {"ms_per_step": round(tsum[k] / args.steps, 4), "GB_per_s": round(g_, 1),
+                             "frac_of_peak": round(g_ / peak, 4), "bytes_per_param": bpp}
+            if w16 and k in traffic_of:
+                trs = [profiled_traffic(t) for t in traffic_of[k]]
+                unfused[name]["traffic_per_element"] = (round(sum(t["dram_bytes_per_element"] for t in trs), 3)
+                                                        if all(trs) else None)
+    else:
+        unfused = dict(return_unfused)
     unfused["how"] = ("reduce_scatter_avg and allreduce_avg: the grouped calls (zr_reduce_scatter_avg_range, "
                       "zr_allreduce_avg_range) over one contiguous buffer per rank holding every bucket; "
                       "*_per_bucket: one zr_reduce_scatter_avg / zr_allreduce_avg call per bucket of the same buffer")
