@@ -311,7 +311,10 @@ def test_fused_without_optional_outputs_and_unfused_agree(zr, world, seed, n, hi
 
 @pytest.mark.parametrize("world,seed,n,hi,B", CASES)
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_allreduce_avg(zr, world, seed, n, hi, B, dtype):
+@pytest.mark.parametrize("outputs", ["random_phases", "one_phase"])
+def test_allreduce_avg(zr, world, seed, n, hi, B, dtype, outputs):
+    """Outputs at random 16-byte phases and at one shared phase (then every
+    output's stores are aligned like replica 0's)."""
     rng, numel, lay = _case(world, seed, n, hi, B)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     es = 2 if dtype == "bf16" else 4
@@ -320,7 +323,8 @@ def test_allreduce_avg(zr, world, seed, n, hi, B, dtype):
     for b in range(min(lay.n_buckets, 3)):
         _, nb = lay.bucket(b)
         vals, dev = _buckets_on_device(rng, lay, b, world, tdt, es)
-        outs = [Guarded(nb, torch.float32, ph) for ph in _rand_phases(rng, world, 4)]
+        phases = _rand_phases(rng, world, 4) if outputs == "random_phases" else [int(rng.integers(0, 4))] * world
+        outs = [Guarded(nb, torch.float32, ph) for ph in phases]
         zr.zr_allreduce_avg(zl, b, [d.view for d in dev], scale, [o.view for o in outs])
         torch.cuda.synchronize()
         want = oracle.allreduce_avg(world, vals, scale)
