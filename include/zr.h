@@ -34,6 +34,11 @@
  *    such a chunk never crosses a page, so this cannot fault.
  *  - "host array of device pointers": a host array (read during the call
  *    only) whose entries are device addresses.
+ *  - A device address may point into pinned (page-locked) host memory, which
+ *    the CUDA runtime maps into the device's address space at the same
+ *    address: the kernels then read or write it in place over the host link
+ *    (for example a direct plan over host-resident gradients, with the bf16
+ *    parameters written to a pinned host buffer), at the link's bandwidth.
  *  - Kernels are enqueued on `stream` (NULL = the legacy default stream) and
  *    the call returns without synchronising. Launch errors are reported;
  *    errors of the asynchronous execution surface at the caller's next

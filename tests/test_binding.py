@@ -120,3 +120,26 @@ def test_pointer_array_from_a_generator_keeps_every_tensor():
     del arr
     gc.collect()
     assert all(r() is None for r in made)
+
+
+class FakeHostTensor(FakeTensor):
+    def __init__(self, addr, pinned):
+        super().__init__(addr)
+        self.is_cuda = False
+        self._pinned = pinned
+
+    def is_pinned(self):
+        return self._pinned
+
+
+def test_pinned_host_tensors_pass_and_pageable_ones_are_refused():
+    """Pinned host memory is mapped into the device's address space, so the
+    binding hands its address over as it does a device tensor's; a pageable CPU
+    tensor is refused before any call."""
+    from zero_partition_aware_gb300 import build
+    build.build()
+    from zero_partition_aware_gb300 import zr
+    arr = zr.PtrArray([FakeTensor(0x5000000), FakeHostTensor(0x6000000, pinned=True)])
+    assert [int(a) for a in arr.array] == [0x5000000, 0x6000000]
+    with pytest.raises(ValueError, match="pageable"):
+        zr.PtrArray([FakeHostTensor(0x6000000, pinned=False)])

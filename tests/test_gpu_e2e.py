@@ -150,3 +150,47 @@ def test_overlapped_pack_and_fused_equal_the_oracle(mods, world, n, hi, B, flat_
     for r in range(world):
         for x, y in ((a.master[r], b.master[r]), (a.m[r], b.m[r]), (a.v[r], b.v[r])):
             assert np.array_equal(_bits(x), _bits(y)), r
+
+
+@pytest.mark.parametrize("world,n,hi,B", [(4, 40, 30_000, 60_000), (16, 120, 200_000, 1 << 21)])
+def test_host_resident_gradients_equal_the_oracle(mods, world, n, hi, B):
+    """The direct step reading every rank's gradients in place from pinned host
+    memory (a plan over pinned host tensors at random element phases) and
+    writing the bf16 params into a pinned host buffer, two steps in a row, equals
+    the oracle's two steps bit for bit; the device parameter buffer is left
+    alone."""
+    engine, zr = mods
+    rng = np.random.default_rng(300 + world)
+    numel = W.random_numels(rng, n, 1, hi)
+    wl = W.Workload("zc", tuple(numel), world, B, ("normal", 1e-2), 0.02, ("absnormal", 1e-4), W.AdamW(step=4))
+    inp = W.draw_inputs(wl, "cuda", seed=world + 1)
+    hp = W.AdamW(step=4)
+    g = engine.DPGroup(numel, world, B, device="cuda")
+    g.load_flat(inp["master"], inp["m"], inp["v"])
+    L = g.layout
+    keep, rows = [], []
+    for k in range(world):
+        flat = inp["grads"][k][0].cpu()
+        row = []
+        for i, c in enumerate(numel):
+            ph = int(rng.integers(0, 8))
+            t = torch.empty(c + 8, dtype=torch.bfloat16).pin_memory()
+            s0 = L.param(i)[0]
+            t[ph:ph + c].copy_(flat[s0:s0 + c])
+            keep.append(t)
+            row.append(t[ph:ph + c])
+        rows.append(row)
+    plan = g.direct_plan(g.grad_table(rows))
+    param_host = torch.full((L.P + 8,), -1, dtype=torch.int16).pin_memory().view(torch.bfloat16)
+    g.param.view(torch.int16).fill_(7)
+    for _ in range(2):
+        g.step_direct(plan, hp, param_out=param_host)
+    torch.cuda.synchronize()
+    lay, p, m_, v_, param = _oracle_steps(numel, world, B, [inp["grads"][k][0] for k in range(world)],
+                                          inp["master"], inp["m"], inp["v"], hp, 2)
+    assert np.array_equal(_bits(param_host[: L.P]).view(np.uint16), param), "params in host memory"
+    assert np.all(_bits(param_host[L.P:]) == -1), "wrote past the parameter buffer"
+    assert np.all(_bits(g.param[: L.P]) == 7), "the device parameter buffer was written"
+    for r in range(world):
+        for dev, ref, nm in ((g.master[r], p[r], "master"), (g.m[r], m_[r], "m"), (g.v[r], v_[r], "v")):
+            assert np.array_equal(_bits(dev).view(np.uint32), ref.view(np.uint32)), f"{nm} of rank {r}"

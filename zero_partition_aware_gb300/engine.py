@@ -187,17 +187,27 @@ class DPGroup:
         zr.zr_step_direct(plan, b, self.scale, self._p_master, self._p_m, self._p_v, hp,
                           self.param if write_param else None, shard_grad_out, stream=stream)
 
-    def step_direct(self, plan: zr.DirectPlan, hp, stream=None, per_bucket: bool = False) -> None:
+    def step_direct(self, plan: zr.DirectPlan, hp, stream=None, per_bucket: bool = False,
+                    param_out: Optional[torch.Tensor] = None) -> None:
         """Steps 1-4 for every bucket in one pass each, no bucket buffer: one
         zr_step_direct_range call, which groups consecutive buckets into as few
         launches as it can (per_bucket: one zr_step_direct call per bucket, as a
-        step that reduces buckets while backward fills them runs)."""
+        step that reduces buckets while backward fills them runs).
+
+        The plan's gradient tensors may be pinned host tensors, and param_out
+        (bf16, at least P elements; default: self.param) a pinned host tensor:
+        the kernels then read the gradients and write the params in place over
+        the host link, with no copy and no staging buffer."""
+        param = self.param if param_out is None else param_out
+        if param_out is not None and (param_out.dtype != torch.bfloat16 or param_out.numel() < self.layout.P):
+            raise ValueError("param_out must be bf16 with at least P elements")
         if per_bucket:
             for b in range(self.layout.n_buckets):
-                self.direct(b, plan, hp, stream=stream)
+                zr.zr_step_direct(plan, b, self.scale, self._p_master, self._p_m, self._p_v, hp, param,
+                                  None, stream=stream)
             return
         zr.zr_step_direct_range(plan, 0, self.layout.n_buckets, self.scale, self._p_master, self._p_m, self._p_v,
-                                hp, self.param, stream=stream)
+                                hp, param, stream=stream)
 
     # ---- the step with a global gradient check ---------------------------------------
     def grad_shards(self) -> List[torch.Tensor]:

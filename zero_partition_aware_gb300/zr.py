@@ -158,14 +158,17 @@ def _check(rc: int, what: str):
 # ----------------------------------------------------------------------------
 
 def _addr(x) -> Optional[int]:
-    """Device address of a tensor, or an int address, or None."""
+    """Device address of a tensor, or an int address, or None. A pinned
+    (page-locked) CPU tensor counts: pinned host memory is mapped into the
+    device's address space at the same address, so kernels read and write it in
+    place over the host link."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
     if hasattr(x, "data_ptr"):
-        if not x.is_cuda:
-            raise ValueError("libzr takes CUDA tensors; got a CPU tensor")
+        if not x.is_cuda and not x.is_pinned():
+            raise ValueError("libzr takes CUDA tensors or pinned CPU tensors; got a pageable CPU tensor")
         if not x.is_contiguous():
             raise ValueError("libzr takes contiguous tensors")
         return x.data_ptr()
