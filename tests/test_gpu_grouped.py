@@ -54,6 +54,8 @@ CASES = {
     "random32": (32, 200, 30_000, 250_000, "random"),
     "world40": (40, 80, 5000, 60_000, None),         # above the copy pipeline's 32: per-bucket register kernel
     "one_per_bucket": (4, 60, 3000, 1, None),        # every param its own bucket: many buckets per launch
+    "world3": (3, 120, 20_000, 150_000, None),        # the register kernels' side of the routing
+    "world5": (5, 120, 20_000, 150_000, "reverse"),   # the pipeline's side, with a one-replica last unit
 }
 
 
