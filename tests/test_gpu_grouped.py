@@ -38,7 +38,7 @@ def _bits(t):
 
 
 def _dev(a: np.ndarray, phase: int, keep: list):
-    dt = torch.bfloat16 if a.dtype == np.uint16 else torch.float32
+    dt = {np.dtype(np.uint16): torch.bfloat16, np.dtype(np.float16): torch.float16}.get(a.dtype, torch.float32)
     base = torch.zeros(a.size + phase + 8, dtype=dt, device="cuda")
     v = base[phase:phase + a.size]
     src = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
@@ -70,13 +70,18 @@ def _setup(name, dtype):
         order = [int(x) for x in rng.permutation(n)]
     lay = oracle.layout(numel, world, B, order=order)
     raw = [[(rng.standard_normal(k) * 1e-2).astype(np.float32) for k in numel] for _ in range(world)]
-    grads = [[oracle.f32_to_bf16(x) for x in row] for row in raw] if dtype == "bf16" else raw
+    if dtype == "bf16":
+        grads = [[oracle.f32_to_bf16(x) for x in row] for row in raw]
+    elif dtype == "fp16":  # numpy's conversion rounds to nearest even
+        grads = [[x.astype(np.float16) for x in row] for row in raw]
+    else:
+        grads = raw
     packs = [oracle.bucket_pack(lay, b, grads) for b in range(lay.n_buckets)]
     bufs = [np.concatenate([packs[b][k] for b in range(lay.n_buckets)]) for k in range(world)]
     return rng, numel, order, lay, packs, bufs
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "fp16"])
 @pytest.mark.parametrize("name", list(CASES))
 def test_grouped_reduce_scatter_and_allreduce_equal_the_oracle(zr, name, dtype):
     rng, numel, order, lay, packs, bufs = _setup(name, dtype)
