@@ -759,7 +759,7 @@ def run_e2e(args, wl, grp, arenas, dplan, hp, stream, nranks, dist):
         lo[b] = offs[i] if lo[b] is None else lo[b]
         hi[b] = offs[i] + n
     h2d_pairs = [[(h[lo[b]:hi[b]], a[lo[b]:hi[b]]) for h, a in zip(host, arenas)] for b in range(L.n_buckets)]
-    h2d = sum((hi[b] - lo[b]) * arenas[0].element_size() for b in range(L.n_buckets)) * len(arenas)
+    h2d = sum(hs.numel() * hs.element_size() for pairs in h2d_pairs for hs, _ in pairs)  # the bytes copied
     d2h = out_host.numel() * out_host.element_size()
     cs, ds = torch.cuda.Stream(), torch.cuda.Stream()
 

@@ -56,8 +56,9 @@ def _assert_oracle(grp, lay, p, m, v, param, what):
             assert np.array_equal(_bits(dev).view(np.uint32), ref.view(np.uint32)), f"{what}: {nm} of rank {r}"
 
 
+@pytest.mark.parametrize("grouped", [False, True], ids=["per_bucket", "groups_of_3"])
 @pytest.mark.parametrize("world,n,hi,B", [(4, 40, 30_000, 60_000), (16, 120, 200_000, 1 << 21)])
-def test_from_host_equals_device_resident(mods, world, n, hi, B):
+def test_from_host_equals_device_resident(mods, world, n, hi, B, grouped):
     engine, zr = mods
     rng = np.random.default_rng(world)
     numel = W.random_numels(rng, n, 1, hi)
@@ -91,14 +92,17 @@ def test_from_host_equals_device_resident(mods, world, n, hi, B):
         b = L.param(i)[1]
         lo[b] = offs[i] if lo[b] is None else lo[b]
         hiw[b] = offs[i] + k
-    pairs = [[(h[lo[b]:hiw[b]], d[lo[b]:hiw[b]]) for h, d in zip(host, dev)] for b in range(L.n_buckets)]
+    # per bucket, or groups of three consecutive buckets copied as one range per rank
+    groups = [(b, min(b + 3, L.n_buckets)) for b in range(0, L.n_buckets, 3)] if grouped else None
+    spans = groups or [(b, b + 1) for b in range(L.n_buckets)]
+    pairs = [[(h[lo[b0]:hiw[b1 - 1]], d[lo[b0]:hiw[b1 - 1]]) for h, d in zip(host, dev)] for b0, b1 in spans]
     param_host = torch.full((L.P,), -1, dtype=torch.int16).pin_memory().view(torch.bfloat16)
     for step in range(2):  # the second step reuses the device arenas and the host buffer
         if step:
             for d in dev:
                 d.fill_(float("nan"))
             param_host.view(torch.int16).fill_(-1)
-        got.step_direct_from_host(got_plan, hp, pairs, param_host)
+        got.step_direct_from_host(got_plan, hp, pairs, param_host, groups=groups)
     torch.cuda.synchronize()
     flat = [torch.cat([a[o:o + k] for o, k in zip(offs, numel)]) for a in arenas]
     lay, p, m_, v_, param = _oracle_steps(numel, world, B, flat, master, m, v, hp, 2)

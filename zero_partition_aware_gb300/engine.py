@@ -256,13 +256,17 @@ class DPGroup:
 
     def step_direct_from_host(self, plan: zr.DirectPlan, hp, h2d: Sequence[Sequence[tuple]],
                               param_host: Optional[torch.Tensor] = None, stream=None,
-                              copy_stream=None, d2h_stream=None) -> None:
+                              copy_stream=None, d2h_stream=None, groups: Optional[Sequence[tuple]] = None) -> None:
         """Every bucket with its gradients arriving from host memory, pipelined
         over three streams: while bucket b's step runs, bucket b+1's gradients
         are copied in and bucket b-1's bf16 params are copied out.
 
         h2d[b]: (host_slice, device_slice) tensor pairs that must be resident
         before bucket b's step (pinned host memory for asynchronous copies).
+        groups: optional [(first, end)] runs of consecutive buckets covering
+        them all in order; then h2d[g] holds group g's pairs, each group is one
+        zr_step_direct_range call and one parameter copy, and the pipeline moves
+        fewer, larger copies.
         param_host: pinned bf16 [P] receiving the full parameter buffer, or None.
         Work is ordered after everything already queued on `stream`, and
         `stream` waits for all of it at the end."""
@@ -273,14 +277,25 @@ class DPGroup:
         ds.wait_stream(cur)
         L = self.layout
         spans = self.bucket_flat_spans()
-        for b in range(L.n_buckets):
+        if groups is None:
+            groups = [(b, b + 1) for b in range(L.n_buckets)]
+        elif [b for g in groups for b in range(g[0], g[1])] != list(range(L.n_buckets)):
+            raise ValueError("groups must cover the buckets in order")
+        if len(h2d) != len(groups):
+            raise ValueError("h2d needs one entry per bucket (or per group)")
+        for g, (b0, b1) in enumerate(groups):
             with torch.cuda.stream(cs):
-                for hs, dv in h2d[b]:
+                for hs, dv in h2d[g]:
                     dv.copy_(hs, non_blocking=True)
             cur.wait_stream(cs)
-            self.direct(b, plan, hp, stream=cur)
+            if b1 - b0 == 1:
+                self.direct(b0, plan, hp, stream=cur)
+            else:
+                zr.zr_step_direct_range(plan, b0, b1 - b0, self.scale, self._p_master, self._p_m, self._p_v, hp,
+                                        self.param, stream=cur)
             if param_host is not None and spans is not None:
-                lo, hi = spans[b]
+                # consecutive buckets hold adjacent param ranges (in either order)
+                lo, hi = min(spans[b][0] for b in range(b0, b1)), max(spans[b][1] for b in range(b0, b1))
                 ds.wait_stream(cur)
                 with torch.cuda.stream(ds):
                     param_host[lo:hi].copy_(self.param[lo:hi], non_blocking=True)
