@@ -509,8 +509,9 @@ typedef struct {
 
 typedef struct zr_gradcheck zr_gradcheck;
 
-/* Allocates on the current device the check's sums (32 KB, zeroed) and its
- * outcome (coef = 1, skip = 0 until the first finalize). */
+/* Allocates on the current device the check's sums (65,536 per-block slots
+ * and the finalize's scratch, about 1 MB, zeroed) and its outcome (coef = 1,
+ * skip = 0 until the first finalize). */
 int zr_gradcheck_create(zr_gradcheck **out);
 int zr_gradcheck_destroy(zr_gradcheck *chk);
 
