@@ -133,13 +133,22 @@ class FakeHostTensor(FakeTensor):
 
 
 def test_pinned_host_tensors_pass_and_pageable_ones_are_refused():
-    """Pinned host memory is mapped into the device's address space, so the
-    binding hands its address over as it does a device tensor's; a pageable CPU
-    tensor is refused before any call."""
+    """Pinned host memory that the runtime has mapped into the device's address
+    space passes the binding as a device tensor does; the binding asks the
+    library once per 2 MB page (zr_host_mapped) and refuses an unmapped page, or
+    a pageable CPU tensor, before any call. With no GPU here the library's
+    answer is 'not mapped', so the mapped case is seeded in the binding's cache."""
     from zero_partition_aware_gb300 import build
     build.build()
     from zero_partition_aware_gb300 import zr
-    arr = zr.PtrArray([FakeTensor(0x5000000), FakeHostTensor(0x6000000, pinned=True)])
-    assert [int(a) for a in arr.array] == [0x5000000, 0x6000000]
+    zr._MAPPED[0x6000000 >> 21] = True
+    try:
+        arr = zr.PtrArray([FakeTensor(0x5000000), FakeHostTensor(0x6000000, pinned=True)])
+        assert [int(a) for a in arr.array] == [0x5000000, 0x6000000]
+    finally:
+        zr._MAPPED.pop(0x6000000 >> 21, None)
     with pytest.raises(ValueError, match="pageable"):
         zr.PtrArray([FakeHostTensor(0x6000000, pinned=False)])
+    with pytest.raises(ValueError, match="not mapped"):
+        zr.PtrArray([FakeHostTensor(0x7200000, pinned=True)])
+    zr._MAPPED.pop(0x7200000 >> 21, None)

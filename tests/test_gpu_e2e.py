@@ -198,3 +198,22 @@ def test_host_resident_gradients_equal_the_oracle(mods, world, n, hi, B):
     for r in range(world):
         for dev, ref, nm in ((g.master[r], p[r], "master"), (g.m[r], m_[r], "m"), (g.v[r], v_[r], "v")):
             assert np.array_equal(_bits(dev).view(np.uint32), ref.view(np.uint32)), f"{nm} of rank {r}"
+
+
+def test_host_mapped_tells_pinned_from_pageable(mods):
+    """zr_host_mapped answers 1 for pinned host memory (mapped at the same
+    address) and 0 for a pageable numpy buffer, and the refused lookup leaves
+    no pending CUDA error behind: the next library launch succeeds."""
+    import ctypes
+    engine, zr = mods
+    pinned = torch.zeros(1 << 20, dtype=torch.float32).pin_memory()
+    pageable = np.zeros(1 << 20, np.float32)
+    m = ctypes.c_int32(-1)
+    assert zr._lib.zr_host_mapped(pinned.data_ptr(), ctypes.byref(m)) == zr.ZR_OK and m.value == 1
+    assert zr._lib.zr_host_mapped(pageable.ctypes.data, ctypes.byref(m)) == zr.ZR_OK and m.value == 0
+    acc = torch.zeros(1 << 20, device="cuda")
+    zr.zr_grad_accumulate(acc, torch.ones(1 << 20, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert float(acc.sum()) == float(1 << 20)
+    with pytest.raises(ValueError, match="pageable"):
+        zr.zr_grad_accumulate(acc, torch.ones(1 << 20, dtype=torch.bfloat16))

@@ -102,6 +102,7 @@ _SIGS = {
     "zr_pack_plan_destroy": (ctypes.c_int, [_vp]),
     "zr_bucket_pack_planned": (ctypes.c_int, [_vp, _i64, _vp]),
     "zr_bucket_pack_noalloc": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
+    "zr_host_mapped": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "zr_grad_accumulate": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_grad_accumulate_first": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_reduce_scatter_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
@@ -157,6 +158,20 @@ def _check(rc: int, what: str):
 # Marshalling helpers
 # ----------------------------------------------------------------------------
 
+_MAPPED = {}  # host page -> mapped into the device's address space (checked once per page)
+
+
+def _check_mapped(ptr: int) -> None:
+    page = ptr >> 21
+    ok = _MAPPED.get(page)
+    if ok is None:
+        m = ctypes.c_int32(0)
+        _check(_lib.zr_host_mapped(ptr, ctypes.byref(m)), "zr_host_mapped")
+        ok = _MAPPED[page] = bool(m.value)
+    if not ok:
+        raise ValueError("pinned host memory at this address is not mapped into the device's address space")
+
+
 def _addr(x) -> Optional[int]:
     """Device address of a tensor, or an int address, or None. A pinned
     (page-locked) CPU tensor counts: pinned host memory is mapped into the
@@ -167,8 +182,10 @@ def _addr(x) -> Optional[int]:
     if isinstance(x, int):
         return x
     if hasattr(x, "data_ptr"):
-        if not x.is_cuda and not x.is_pinned():
-            raise ValueError("libzr takes CUDA tensors or pinned CPU tensors; got a pageable CPU tensor")
+        if not x.is_cuda:
+            if not x.is_pinned():
+                raise ValueError("libzr takes CUDA tensors or pinned CPU tensors; got a pageable CPU tensor")
+            _check_mapped(x.data_ptr())
         if not x.is_contiguous():
             raise ValueError("libzr takes contiguous tensors")
         return x.data_ptr()
