@@ -148,12 +148,12 @@ int zr_version(void);
  * variable is read at every attempt; unset or 0, it has no effect. */
 int64_t zr_launch_count(void);
 
-/* Whether host address p lies in pinned host memory that the CUDA runtime has
- * mapped into the current device's address space at the same address (the
+/* Whether the current device reaches host address p at the same address (the
  * condition for passing it where the library takes device pointers): *mapped
- * = 1 if so, 0 otherwise (pageable memory, or a runtime without such mapping).
- * Returns ZR_ERR_INVALID_ARG if mapped is NULL, else ZR_OK; the runtime's
- * answer for an unmapped address is not left behind as a pending error. */
+ * = 1 if the CUDA runtime reports p's device address as p itself (pinned host
+ * memory it has mapped; on systems whose device uses the host's page tables,
+ * any host memory), 0 otherwise. Returns ZR_ERR_INVALID_ARG if mapped is
+ * NULL, else ZR_OK; a refused lookup is not left behind as a pending error. */
 int zr_host_mapped(const void *p, int32_t *mapped);
 
 /* ---- layout (host only) ------------------------------------------------ */

@@ -200,17 +200,21 @@ def test_host_resident_gradients_equal_the_oracle(mods, world, n, hi, B):
             assert np.array_equal(_bits(dev).view(np.uint32), ref.view(np.uint32)), f"{nm} of rank {r}"
 
 
-def test_host_mapped_tells_pinned_from_pageable(mods):
+def test_host_mapped_answers_and_leaves_no_error(mods):
     """zr_host_mapped answers 1 for pinned host memory (mapped at the same
-    address) and 0 for a pageable numpy buffer, and the refused lookup leaves
-    no pending CUDA error behind: the next library launch succeeds."""
+    address). For a pageable numpy buffer the answer depends on the system (a
+    device that uses the host's page tables reaches any host memory at the same
+    address); either way the call succeeds and leaves no pending CUDA error
+    behind: the next library launch succeeds. The binding itself refuses
+    pageable tensors whatever the system allows."""
     import ctypes
     engine, zr = mods
     pinned = torch.zeros(1 << 20, dtype=torch.float32).pin_memory()
     pageable = np.zeros(1 << 20, np.float32)
     m = ctypes.c_int32(-1)
     assert zr._lib.zr_host_mapped(pinned.data_ptr(), ctypes.byref(m)) == zr.ZR_OK and m.value == 1
-    assert zr._lib.zr_host_mapped(pageable.ctypes.data, ctypes.byref(m)) == zr.ZR_OK and m.value == 0
+    assert zr._lib.zr_host_mapped(pageable.ctypes.data, ctypes.byref(m)) == zr.ZR_OK and m.value in (0, 1)
+    assert zr._lib.zr_host_mapped(pageable.ctypes.data, None) == zr.ZR_ERR_INVALID_ARG
     acc = torch.zeros(1 << 20, device="cuda")
     zr.zr_grad_accumulate(acc, torch.ones(1 << 20, dtype=torch.bfloat16, device="cuda"))
     torch.cuda.synchronize()
