@@ -69,7 +69,7 @@ extern "C" {
 #define ZR_ERR_ALIGN (-4)        /* a device pointer is not element-aligned */
 #define ZR_ERR_TIMEOUT (-5)      /* reserved: a bounded device wait ran out */
 #define ZR_ERR_STATE (-6)        /* no usable CUDA device / wrong device state */
-#define ZR_ERR_UNSUPPORTED (-7)  /* a size beyond what this build supports */
+#define ZR_ERR_UNSUPPORTED (-7)  /* a size beyond what the library supports */
 
 /* Largest world (emulated data-parallel size) the kernels accept. */
 #define ZR_MAX_WORLD 1024
