@@ -476,7 +476,7 @@ def run_gpu(args, rank, nranks, local, dist):
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def unfused_step(timed):
-        e = [ev() for _ in range(5)]
+        e = [ev() for _ in range(6)]
         e[0].record(stream)
         _zr.zr_reduce_scatter_avg_range(L, 0, nbk, p_gbuf, grp.scale, grp._p_grad, dtype=grp.zr_dtype, stream=stream)
         e[1].record(stream)
@@ -486,7 +486,11 @@ def run_gpu(args, rank, nranks, local, dist):
         e[3].record(stream)
         _zr.zr_gather_cast_bf16(L, grp._p_master, grp.param, stream=stream)
         e[4].record(stream)
-        timed += [("rs", e[0], e[1]), ("ar", e[1], e[2]), ("adam", e[2], e[3]), ("cast", e[3], e[4])]
+        _zr.zr_rs_adam_fused_range(L, 0, nbk, p_gbuf, grp.scale, grp._p_master, grp._p_m, grp._p_v, hp, grp.param,
+                                   dtype=grp.zr_dtype, stream=stream)
+        e[5].record(stream)
+        timed += [("rs", e[0], e[1]), ("ar", e[1], e[2]), ("adam", e[2], e[3]), ("cast", e[3], e[4]),
+                  ("fused_range", e[4], e[5])]
 
     def per_bucket_rs(timed):  # the per-bucket calls over the same buffer, for comparison
         for b in range(nbk):
@@ -512,15 +516,17 @@ def run_gpu(args, rank, nranks, local, dist):
             per_bucket_rs(marks)
         torch.cuda.synchronize()
     if return_unfused is None:
-        tsum = {k: 0.0 for k in ("rs", "ar", "adam", "cast", "rs_pb", "ar_pb")}
+        tsum = {k: 0.0 for k in ("rs", "ar", "adam", "cast", "fused_range", "rs_pb", "ar_pb")}
         for k, a, b_ in marks:
             tsum[k] += a.elapsed_time(b_)
         unfused = {}
         w16 = wl.world == 16
         traffic_of = {"rs": ["reduce_scatter_range_bf16_w16"], "adam": ["adam_shard_w16"],
-                      "ar": ["allreduce_pass_bf16_w16", "allreduce_bcast_w16"]}
+                      "ar": ["allreduce_pass_bf16_w16", "allreduce_bcast_w16"],
+                      "fused_range": ["rs_adam_fused_bf16_w16"]}
         for k, name, bpp in (("rs", "reduce_scatter_avg", 2 * wl.world + 4), ("adam", "adam_shard_step", 28),
                              ("cast", "gather_cast_bf16", 6), ("ar", "allreduce_avg", 6 * wl.world),
+                             ("fused_range", "rs_adam_fused_range", 2 * wl.world + 26),
                              ("rs_pb", "reduce_scatter_avg_per_bucket", 2 * wl.world + 4),
                              ("ar_pb", "allreduce_avg_per_bucket", 6 * wl.world)):
             g_ = gbs(L.P * bpp, tsum[k])
@@ -532,9 +538,10 @@ def run_gpu(args, rank, nranks, local, dist):
                                                         if all(trs) else None)
     else:
         unfused = dict(return_unfused)
-    unfused["how"] = ("reduce_scatter_avg and allreduce_avg: the grouped calls (zr_reduce_scatter_avg_range, "
-                      "zr_allreduce_avg_range) over one contiguous buffer per rank holding every bucket; "
-                      "*_per_bucket: one zr_reduce_scatter_avg / zr_allreduce_avg call per bucket of the same buffer")
+    unfused["how"] = ("reduce_scatter_avg, allreduce_avg and rs_adam_fused_range: the grouped calls "
+                      "(zr_reduce_scatter_avg_range, zr_allreduce_avg_range, zr_rs_adam_fused_range) over one "
+                      "contiguous buffer per rank holding every bucket; *_per_bucket: one zr_reduce_scatter_avg / "
+                      "zr_allreduce_avg call per bucket of the same buffer")
     del ar_out, p_ar, gbuf, p_gbuf
     torch.cuda.empty_cache()
 

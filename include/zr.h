@@ -375,6 +375,21 @@ int zr_rs_adam_fused(const zr_layout *layout, int64_t bucket, const void *const 
                      float *const *shard_grad_out, zr_stream stream);
 
 /*
+ * zr_rs_adam_fused for the buckets [bucket_first, bucket_first + bucket_count)
+ * of one contiguous gradient buffer per rank, laid out as for
+ * zr_reduce_scatter_avg_range (grad_buf[k]: rank k's buffer, every bucket back
+ * to back in bucket order; only the range's buckets are read). Consecutive
+ * buckets share launches up to 2^26 elements, and the results equal one
+ * zr_rs_adam_fused call per bucket (bucket_in[k] = grad_buf[k] + the bucket's
+ * offset), bit for bit. master, m, v, param_bf16 and shard_grad_out as for
+ * zr_rs_adam_fused.
+ */
+int zr_rs_adam_fused_range(const zr_layout *layout, int64_t bucket_first, int64_t bucket_count,
+                           const void *const *grad_buf, zr_dtype dtype, float scale, float *const *master,
+                           float *const *m, float *const *v, const zr_adamw *hp, void *param_bf16,
+                           float *const *shard_grad_out, zr_stream stream);
+
+/*
  * zr_rs_adam_fused with the last micro-step's accumulation folded in ([MG]
  * §"四步接力": every micro-step's 16-bit grad is added into the fp32 main_grad
  * before the bucket is reduced; §"通信模式"): for bucket position e,

@@ -177,3 +177,40 @@ def test_fused_on_buckets_of_many_runs(zr, world, n, hi, dt):
     for r in range(world):
         for a, b_ in ((P_[r], p[r]), (M_[r], m[r]), (V_[r], v[r]), (G_[r], g_ref[r])):
             assert np.array_equal(_bits(a), b_.view(np.uint32)), r
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("name", ["flat16", "reverse8", "world3", "world5", "world40", "one_per_bucket"])
+def test_grouped_fused_step_equals_the_oracle(zr, name, dtype):
+    """zr_rs_adam_fused_range over a contiguous buffer per rank, on the whole
+    range and on an inner one, equals the oracle's fused step per bucket:
+    master, m, v, the averaged gradient and the bf16 params, bit for bit, and
+    nothing outside the range's partition slices changes."""
+    rng, numel, order, lay, packs, bufs = _setup(name, dtype)
+    world, nb = lay.world, lay.n_buckets
+    zl = zr.Layout(numel, world, CASES[name][3], arrival=order)
+    keep = []
+    x = [_dev(a, int(rng.integers(0, 8)), keep) for a in bufs]
+    scale = float(np.float32(1.0 / world))
+    hp = W.AdamW(step=3)
+    lo, hi = (0, nb) if nb < 3 else (1, nb - 1)
+    for first, count in ((0, nb), (lo, hi - lo)):
+        flat = lambda std: np.concatenate([(rng.standard_normal(lay.T) * std).astype(np.float32),
+                                           np.zeros(lay.P - lay.T, np.float32)])
+        p, m, v = ([np.ascontiguousarray(a) for a in np.split(s_, world)]
+                   for s_ in (flat(0.02), np.abs(flat(1e-4)), np.abs(flat(1e-4))))
+        P_ = [_dev(a, int(rng.integers(0, 4)), keep) for a in p]
+        M_ = [_dev(a, int(rng.integers(0, 4)), keep) for a in m]
+        V_ = [_dev(a, int(rng.integers(0, 4)), keep) for a in v]
+        G_ = [_dev(np.full(lay.S, np.nan, np.float32), int(rng.integers(0, 4)), keep) for _ in range(world)]
+        param = torch.full((lay.P,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        zr.zr_rs_adam_fused_range(zl, first, count, x, scale, P_, M_, V_, hp, param, G_)
+        torch.cuda.synchronize()
+        rparam = np.full(lay.P, 0xFFFF, np.uint16)
+        g_ref = [np.full(lay.S, np.nan, np.float32) for _ in range(world)]
+        for b in range(first, first + count):
+            oracle.rs_adam_fused(lay, b, packs[b], scale, p, m, v, hp, rparam, g_ref)
+        assert np.array_equal(_bits(param), rparam), ("params", first, count)
+        for r in range(world):
+            for a, b_ in ((P_[r], p[r]), (M_[r], m[r]), (V_[r], v[r]), (G_[r], g_ref[r])):
+                assert np.array_equal(_bits(a), b_.view(np.uint32)), (first, count, r)

@@ -103,6 +103,8 @@ _SIGS = {
     "zr_bucket_pack_planned": (ctypes.c_int, [_vp, _i64, _vp]),
     "zr_bucket_pack_noalloc": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
     "zr_host_mapped": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
+    "zr_rs_adam_fused_range": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _f32, _vp, _vp, _vp, _vp, _vp,
+                                              _vp, _vp]),
     "zr_grad_accumulate": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_grad_accumulate_first": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _vp]),
     "zr_reduce_scatter_avg": (ctypes.c_int, [_vp, _i64, _vp, ctypes.c_int, _f32, _vp, _vp]),
@@ -497,6 +499,18 @@ def zr_rs_adam_fused(layout: Layout, bucket: int, bucket_in, scale: float, maste
     _check(_lib.zr_rs_adam_fused(layout.handle, int(bucket), px.ptr, d, float(scale), pm.ptr, pmm.ptr, pv.ptr,
                                  ctypes.byref(h), _addr(param_bf16), go.ptr if go is not None else None,
                                  _stream(stream)), "zr_rs_adam_fused")
+
+
+def zr_rs_adam_fused_range(layout: Layout, bucket_first: int, bucket_count: int, grad_buf, scale: float, master,
+                           m, v, hp, param_bf16=None, shard_grad_out=None, dtype=None, stream=None) -> None:
+    """grad_buf: [world] buffers holding the buckets back to back in bucket order."""
+    d = _dtype_of(grad_buf, dtype)
+    h = _hp(hp)
+    px, pm, pmm, pv, go = _ptrs(grad_buf), _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(shard_grad_out)
+    _check(_lib.zr_rs_adam_fused_range(layout.handle, int(bucket_first), int(bucket_count), px.ptr, d, float(scale),
+                                       pm.ptr, pmm.ptr, pv.ptr, ctypes.byref(h), _addr(param_bf16),
+                                       go.ptr if go is not None else None, _stream(stream)),
+           "zr_rs_adam_fused_range")
 
 
 def zr_rs_adam_fused_acc(layout: Layout, bucket: int, main_in, last_in, scale: float, master, m, v, hp,
