@@ -128,6 +128,37 @@ def test_range_norm_pass_equals_oracle(zr, name):
     assert got["sumsq"] == ref.sumsq and got["coef"] == ref.coef  # integer grads, power-of-two world: exact
 
 
+def test_range_norm_pass_repeats_bit_for_bit(zr):
+    """The norm pass over several launches of one call, on non-integer gradients
+    (whose sum depends on the order of the adds): three passes give the same
+    outcome bit for bit, as the launches add to the check's slots in launch
+    order even when a launch starts before the one before it has completed."""
+    rng, numel, order, lay, grads = _setup("many_buckets")
+    world = lay.world
+    zl = zr.Layout(numel, world, CASES["many_buckets"][3], arrival=order)
+    keep = []
+    plan = zr.DirectPlan(zl, [[_dev(g, int(rng.integers(0, 8)), keep) for g in row] for row in grads])
+    g_out = [_dev(np.zeros(lay.S, np.float32), 0, keep) for _ in range(world)]
+    chk = zr.GradCheck()
+    scale = float(np.float32(1.0 / world))
+    outs = []
+    for _ in range(3):
+        n0 = zr.zr_launch_count()
+        zr.zr_rs_direct_norm_range(plan, 0, lay.n_buckets, scale, g_out, chk)
+        launches = zr.zr_launch_count() - n0
+        zr.zr_grad_check_finalize(chk, 1.0)
+        outs.append(zr.zr_gradcheck_read(chk))
+    assert launches > 2
+    assert outs[0] == outs[1] == outs[2]
+    g_ref = [np.zeros(lay.S, np.float32) for _ in range(world)]
+    for b in range(lay.n_buckets):
+        oracle.reduce_scatter_avg(lay, b, oracle.bucket_pack(lay, b, grads), scale, g_ref)
+    for r in range(world):
+        assert np.array_equal(_bits(g_out[r]), g_ref[r].view(np.uint32)), r
+    ref = oracle.grad_check(g_ref, 1.0)
+    assert abs(outs[0]["sumsq"] - ref.sumsq) <= 1e-6 * ref.sumsq
+
+
 def test_range_subsets_and_bad_ranges(zr):
     """Two half ranges equal one full range; out-of-range buckets are refused."""
     rng, numel, order, lay, grads = _setup("many_buckets")
