@@ -455,6 +455,13 @@ int zr_step_direct(const zr_direct_plan *plan, int64_t bucket, float scale, floa
  * a step that runs once every bucket's gradients are ready (after backward,
  * or at a gradient-accumulation boundary); a step that reduces buckets as
  * backward fills them calls zr_step_direct per bucket.
+ * Stream order: the call's first launch starts after all earlier work on
+ * the stream, as any launch does. Each later launch of the same call (other
+ * buckets, other tile counters) is a programmatic dependent of the one
+ * before: its blocks may start while that launch drains, and it completes
+ * only after that launch has. So work queued after the call, and an event
+ * recorded after it, still see the whole call complete; in between, the
+ * call's launches overlap.
  */
 int zr_step_direct_range(const zr_direct_plan *plan, int64_t bucket_first, int64_t bucket_count, float scale,
                          float *const *master, float *const *m, float *const *v, const zr_adamw *hp,
@@ -560,7 +567,10 @@ int zr_rs_direct_norm(const zr_direct_plan *plan, int64_t bucket, float scale, f
                       zr_gradcheck *chk, zr_stream stream);
 
 /* zr_rs_direct_norm for buckets [bucket_first, bucket_first + bucket_count),
- * grouped into launches as zr_step_direct_range groups them. */
+ * grouped into launches as zr_step_direct_range groups them, with the same
+ * stream order (later launches of the call overlap the one before). Each
+ * launch adds its sums to chk only after the launch before it has completed,
+ * so the sums are added in the same order on every call. */
 int zr_rs_direct_norm_range(const zr_direct_plan *plan, int64_t bucket_first, int64_t bucket_count, float scale,
                             float *const *shard_grad, zr_gradcheck *chk, zr_stream stream);
 
