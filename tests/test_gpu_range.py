@@ -159,6 +159,46 @@ def test_range_norm_pass_repeats_bit_for_bit(zr):
     assert abs(outs[0]["sumsq"] - ref.sumsq) <= 1e-6 * ref.sumsq
 
 
+def test_range_step_completes_before_later_work(zr):
+    """A large first launch and small later ones in one range call: work queued
+    on the stream right after the call (device copies, no host wait between)
+    must see every launch's results. A later launch of the call may start while
+    the one before drains, but completes only after it."""
+    world = 8
+    rng = np.random.default_rng(11)
+    numel = [3_000_000] + [int(x) for x in rng.integers(1, 4000, 40)]
+    lay = oracle.layout(numel, world, 1)  # one bucket per param: the big one opens the first launch
+    zl = zr.Layout(numel, world, 1)
+    keep = []
+    raw = [[(rng.standard_normal(k) * 1e-2).astype(np.float32) for k in numel] for _ in range(world)]
+    grads = [[oracle.f32_to_bf16(x) for x in row] for row in raw]
+    plan = zr.DirectPlan(zl, [[_dev(g, 0, keep) for g in row] for row in grads])
+    flat = lambda std: np.concatenate([(rng.standard_normal(lay.T) * std).astype(np.float32),
+                                       np.zeros(lay.P - lay.T, np.float32)])
+    p, m, v = ([np.ascontiguousarray(a) for a in np.split(x, world)]
+               for x in (flat(0.02), np.abs(flat(1e-4)), np.abs(flat(1e-4))))
+    P_ = [_dev(a, 0, keep) for a in p]
+    M_ = [_dev(a, 0, keep) for a in m]
+    V_ = [_dev(a, 0, keep) for a in v]
+    param = torch.zeros(lay.P, dtype=torch.bfloat16, device="cuda")
+    hp = W.AdamW(step=4)
+    scale = float(np.float32(1.0 / world))
+    torch.cuda.synchronize()
+    n0 = zr.zr_launch_count()
+    zr.zr_step_direct_range(plan, 0, lay.n_buckets, scale, P_, M_, V_, hp, param)
+    launches = zr.zr_launch_count() - n0
+    copies = [t.clone() for t in [param] + P_ + M_ + V_]  # queued behind the call
+    torch.cuda.synchronize()
+    assert launches >= 3
+    rparam = np.zeros(lay.P, np.uint16)
+    for b in range(lay.n_buckets):
+        oracle.rs_adam_fused(lay, b, oracle.bucket_pack(lay, b, grads), scale, p, m, v, hp, rparam)
+    assert np.array_equal(_bits(copies[0]), rparam)
+    for r in range(world):
+        for a, b_ in ((copies[1 + r], p[r]), (copies[1 + world + r], m[r]), (copies[1 + 2 * world + r], v[r])):
+            assert np.array_equal(_bits(a), b_.view(np.uint32)), r
+
+
 def test_range_subsets_and_bad_ranges(zr):
     """Two half ranges equal one full range; out-of-range buckets are refused."""
     rng, numel, order, lay, grads = _setup("many_buckets")
