@@ -433,6 +433,13 @@ int zr_rs_adam_fused_acc(const zr_layout *layout, int64_t bucket, const float *c
  * (SMs that run faster take more), and the launch leaves them at zero. Calls whose
  * buckets are disjoint may therefore run on different streams at once; calls
  * that share a bucket must be ordered (they write the same elements anyway).
+ * The gradients may lie in pinned (page-locked, mapped) host memory instead
+ * of device memory, and param_bf16 likewise: the kernels then read and write
+ * them over the host link, with no copy. A plan whose rank-0 first gradient
+ * is such host memory (as the runtime reports it at creation) runs its steps
+ * on plain loads, which draw the host link's rate; device plans run on the
+ * copy pipeline, except the step at world <= 2. Which kernel runs changes no
+ * result.
  * world <= 32 (ZR_ERR_UNSUPPORTED above).
  * master, m, v, shard_grad_out, param_bf16: as for zr_rs_adam_fused.
  */
