@@ -327,6 +327,9 @@ int zr_reduce_scatter_avg(const zr_layout *layout, int64_t bucket, const void *c
  * bucket (bucket_in[k] = grad_buf[k] + that offset), bit for bit.
  * Differs from the per-bucket call only in where the buckets sit: one buffer
  * per rank for the whole range instead of one bucket buffer per call.
+ * Stream order as for zr_step_direct_range: the first launch waits for all
+ * earlier work; later launches of the call (other runs, other outputs) may
+ * start while the one before drains, and complete only after it.
  */
 int zr_reduce_scatter_avg_range(const zr_layout *layout, int64_t bucket_first, int64_t bucket_count,
                                 const void *const *grad_buf, zr_dtype dtype, float scale,
@@ -382,7 +385,7 @@ int zr_rs_adam_fused(const zr_layout *layout, int64_t bucket, const void *const 
  * buckets share launches up to 2^26 elements, and the results equal one
  * zr_rs_adam_fused call per bucket (bucket_in[k] = grad_buf[k] + the bucket's
  * offset), bit for bit. master, m, v, param_bf16 and shard_grad_out as for
- * zr_rs_adam_fused.
+ * zr_rs_adam_fused. Stream order as for zr_reduce_scatter_avg_range.
  */
 int zr_rs_adam_fused_range(const zr_layout *layout, int64_t bucket_first, int64_t bucket_count,
                            const void *const *grad_buf, zr_dtype dtype, float scale, float *const *master,
@@ -498,7 +501,9 @@ int zr_allreduce_avg(const zr_layout *layout, int64_t bucket, const void *const 
  * zr_reduce_scatter_avg_range; out[k] (host array [world] of device pointers,
  * fp32) receives the same bucket-order layout, and only the range's positions
  * are written. Consecutive buckets share launches up to 2^26 elements; the
- * results equal one zr_allreduce_avg call per bucket, bit for bit.
+ * results equal one zr_allreduce_avg call per bucket, bit for bit. The
+ * averaging launches overlap as in zr_reduce_scatter_avg_range; the copy to
+ * the other replicas starts after the last of them has completed.
  */
 int zr_allreduce_avg_range(const zr_layout *layout, int64_t bucket_first, int64_t bucket_count,
                            const void *const *grad_buf, zr_dtype dtype, float scale, float postscale,
