@@ -270,8 +270,7 @@ int zr_bucket_pack_planned(const zr_pack_plan *plan, int64_t bucket, zr_stream s
  * their launch parameters. Nothing is copied from host memory, so the call
  * does not wait for the stream. A bigger bucket returns ZR_ERR_UNSUPPORTED.
  * The first call on a device looks the table's address up
- * (cudaGetSymbolAddress); make that first call before any stream capture. All
- * calls share the table: calls on one stream are ordered, but calls whose work
+ * (cudaGetSymbolAddress). All calls share the table: calls on one stream are ordered, but calls whose work
  * overlaps on the GPU (different streams) race on it.
  */
 int zr_bucket_pack_noalloc(const zr_layout *layout, int64_t bucket, const void *const *grads, zr_dtype dtype,
